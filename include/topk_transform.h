@@ -1,0 +1,134 @@
+/*
+ * topk_transform.h - exact per-row top-k transform of sparse-attention indexer
+ * scores, for NVIDIA GB300 (sm_103a).
+ *
+ * What the operation computes (per row b of a batch):
+ *   L = clamp(seq_lens[b], 0, row_stride)   (raw, paged)
+ *     = max(seq_lens[b], 0)                 (ragged)
+ *   Select the m = min(k, L) positions j < L whose fp32 scores are largest,
+ *   exactly: scores are ranked by the order-preserving 32-bit key of their bit
+ *   pattern (negative values bit-inverted, the others with the sign bit set),
+ *   which is float order with -0.0 just below +0.0 (sglang PR #37591 summary
+ *   page, section "关键源码片段" (code excerpts), order_key32). Among equal keys at
+ *   the threshold the smaller position wins, so the selected set is unique. No
+ *   element is ever dropped, whatever the distribution (PR #37591 page, sections
+ *   "执行摘要" (summary) and "实现拆解" (implementation breakdown) item 1).
+ *   Each selected j is written mapped:
+ *     raw     j
+ *     paged   page_table[b * page_table_stride + j / page_size] * page_size + j % page_size
+ *     ragged  row_starts[b] + j
+ *   and the slots m .. k-1 of the row are written with -1 (sglang PR #36004
+ *   summary page, section "关键源码片段": test_deepseek_v4_topk_transform
+ *   pre-fills the output with -1 and uses an identity page table, under which the
+ *   paged slot equals the token position). The three entry points mirror the
+ *   three API forms named on the PR #37591 page, "实现拆解" item 2.
+ *
+ * Output order: the order of the m positions inside out[b, 0:k) is unspecified;
+ * compare rows as sets. The SET is deterministic.
+ *
+ * Memory and ownership: every pointer argument is device memory owned by the
+ * caller (for example torch tensors passed as data_ptr()). The library never
+ * allocates, frees or synchronises; each call enqueues one kernel on `stream`
+ * (NULL = the legacy default stream) and returns. All inputs must stay valid and
+ * unmodified until that kernel has finished. `out` is fully written, including
+ * the -1 padding, so it need not be pre-filled. The first call on a device sets
+ * kernel attributes on that device; make it before capturing a CUDA graph.
+ *
+ * Layouts (all row-major, int32 unless stated):
+ *   scores      fp32, 4-byte aligned. raw/paged: row b starts at
+ *               scores + b * row_stride (elements); ragged: row b starts at
+ *               scores + row_starts[b]. Any alignment of a row start is accepted.
+ *   seq_lens    [batch]
+ *   page_table  [batch, page_table_stride]; entries are trusted: the entries for
+ *               pages 0 .. ceil(L/page_size)-1 of each row must exist.
+ *   row_starts  [batch], element offsets into `scores`; row_starts[b] + j must
+ *               fit in int32.
+ *   out         [batch, k]
+ *
+ * Errors: host-checkable problems return a status and launch nothing. Values
+ * that live in device memory (seq_lens, page_table, row_starts) are not
+ * validated: seq_lens are clamped as above, the others are trusted. A launch
+ * failure returns TOPK_ERR_CUDA; topk_last_cuda_error() gives the cudaError_t.
+ */
+#ifndef TOPK_TRANSFORM_H_
+#define TOPK_TRANSFORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TOPK_OK = 0,
+  TOPK_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative batch, bad stride or page size */
+  TOPK_ERR_UNSUPPORTED_K = 2,    /* k outside [1, TOPK_MAX_K] */
+  TOPK_ERR_WORKSPACE_TOO_SMALL = 3,
+  TOPK_ERR_CUDA = 4              /* a CUDA runtime call or the launch failed */
+} topk_status_t;
+
+/* Largest supported k. The pages' kernels fix k at 1024 (the legacy
+ * deepseek_v4_topk_transform, PR #36004 page, "关键源码片段", kMaxTopK) and at
+ * 2048 (the exact kernel, PR #37591 page, "实现拆解" item 2, kTopK). Any k in
+ * [1, TOPK_MAX_K] is accepted. */
+#define TOPK_MAX_K 2048
+
+/* Device workspace (bytes) a call with these sizes needs. The kernels keep all
+ * per-row state in shared memory, so this is 0 for every size; the workspace
+ * arguments below exist so that a future global-memory path does not change the
+ * ABI. */
+size_t topk_workspace_bytes(int32_t batch, int64_t max_row_len, int32_t k);
+
+/* Raw form. scores [batch, row_stride] fp32 (row_stride >= 1 elements),
+ * seq_lens [batch], out [batch, k]. `workspace` may be NULL when
+ * `workspace_bytes` is 0. Returns a topk_status_t. */
+int topk_transform_raw(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                       int32_t batch, int32_t k, int32_t* out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Paged form: as raw, each position mapped through the row's page table
+ * (page_size >= 1, page_table_stride >= 1). */
+int topk_transform_paged(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                         const int32_t* page_table, int64_t page_table_stride,
+                         int32_t page_size, int32_t batch, int32_t k, int32_t* out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Ragged form: row b is scores[row_starts[b] .. row_starts[b] + seq_lens[b]) of a
+ * packed buffer; each selected position is written as row_starts[b] + j.
+ * max_row_len_hint (>= 0) is an upper bound of the row lengths, used only to
+ * choose how many CTAs share a row; 0 means "unknown, assume long". */
+int topk_transform_ragged(const float* scores, const int32_t* row_starts,
+                          const int32_t* seq_lens, int64_t max_row_len_hint, int32_t batch,
+                          int32_t k, int32_t* out, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/* A static English description of a status code. */
+const char* topk_status_string(int status);
+
+/* The cudaError_t of the last TOPK_ERR_CUDA returned on this host thread. */
+int topk_last_cuda_error(void);
+
+/* Tuning and test controls (process-wide; each returns the previous value).
+ *
+ * topk_set_row_split(g): number of CTAs (a thread-block cluster) that share one
+ * row: 1, 2, 4, 8 or 16 (other values round down to a power of two); any value
+ * < 1 restores the built-in choice, which depends on batch, row length and SM
+ * count (the row-split heuristic of the PR #37591 page, "关键源码片段",
+ * row_split, restated for a cluster). The environment variable TOPK_ROW_SPLIT
+ * sets the initial value.
+ *
+ * topk_set_tie_capacity(cap): entries of the shared tie buffer, clamped to
+ * [0, TOPK_TIE_CAPACITY_MAX]. Smaller values force the exact position-ordered
+ * rescan for more rows (used by tests); the result never changes. */
+#define TOPK_TIE_CAPACITY_MAX 4096
+int topk_set_row_split(int g);
+int topk_set_tie_capacity(int cap);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* TOPK_TRANSFORM_H_ */

@@ -1,0 +1,204 @@
+"""Exact per-row top-k transform of sparse-attention indexer scores on GB300.
+
+A thin ctypes binding over the C ABI in ``include/topk_transform.h``: the Python
+functions carry the C entry points' names, check and marshal torch tensors, and
+call the library on the tensors' device and the current torch stream. All the
+work runs in the library's sm_103a kernels; there is no fallback. If the library
+has not been built, or a tensor is not on a CUDA device, the call raises.
+
+    out = topk_transform_paged(scores, seq_lens, page_table, page_size=64, k=1024)
+
+``scores`` is fp32 [B, row_stride] with unit inner stride (raw/paged) or a packed
+1-D buffer (ragged). Rows of ``out`` hold the selected positions, mapped, in an
+unspecified order, followed by -1 where a row has fewer than k positions.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
+    "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged",
+    "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity",
+]
+
+TOPK_MAX_K = 2048
+TOPK_TIE_CAPACITY_MAX = 4096
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported k", 3: "workspace too small",
+           4: "CUDA error"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TopkError(RuntimeError):
+    """A non-OK status from the library."""
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it first (python -m "
+                    "sparse_attention_indexer_sm_gb300.build, or __graft_entry__.build())")
+            lib = ctypes.CDLL(path)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            lib.topk_workspace_bytes.restype = sz
+            lib.topk_workspace_bytes.argtypes = [i32, i64, i32]
+            lib.topk_transform_raw.restype = ctypes.c_int
+            lib.topk_transform_raw.argtypes = [vp, i64, vp, i32, i32, vp, vp, sz, vp]
+            lib.topk_transform_paged.restype = ctypes.c_int
+            lib.topk_transform_paged.argtypes = [vp, i64, vp, vp, i64, i32, i32, i32, vp, vp, sz, vp]
+            lib.topk_transform_ragged.restype = ctypes.c_int
+            lib.topk_transform_ragged.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, sz, vp]
+            lib.topk_status_string.restype = ctypes.c_char_p
+            lib.topk_status_string.argtypes = [ctypes.c_int]
+            lib.topk_last_cuda_error.restype = ctypes.c_int
+            lib.topk_last_cuda_error.argtypes = []
+            lib.topk_set_row_split.restype = ctypes.c_int
+            lib.topk_set_row_split.argtypes = [ctypes.c_int]
+            lib.topk_set_tie_capacity.restype = ctypes.c_int
+            lib.topk_set_tie_capacity.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        lib = load_library()
+        msg = lib.topk_status_string(status).decode()
+        if status == 4:
+            msg += f" (cudaError {lib.topk_last_cuda_error()})"
+        raise TopkError(f"{what}: {msg}")
+
+
+def _cuda_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, device=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _vector(t: torch.Tensor, name: str, n: int, device) -> None:
+    _cuda_tensor(t, name, torch.int32, device)
+    if t.dim() != 1 or t.shape[0] != n or (n > 1 and t.stride(0) != 1):
+        raise ValueError(f"{name} must be a contiguous int32 vector of length {n}")
+
+
+def _out(out, batch: int, k: int, device) -> torch.Tensor:
+    if out is None:
+        return torch.empty((batch, k), dtype=torch.int32, device=device)
+    _cuda_tensor(out, "out", torch.int32, device)
+    if tuple(out.shape) != (batch, k) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous int32 tensor of shape ({batch}, {k})")
+    return out
+
+
+def _stream(stream, device) -> int:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _scores_2d(scores: torch.Tensor):
+    _cuda_tensor(scores, "scores", torch.float32)
+    if scores.dim() != 2 or not scores.is_contiguous() or scores.shape[1] < 1:
+        raise ValueError("scores must be a contiguous [batch, row_stride] fp32 tensor, row_stride >= 1")
+    return int(scores.shape[0]), int(scores.shape[1])
+
+
+def topk_workspace_bytes(batch: int, max_row_len: int, k: int) -> int:
+    return int(load_library().topk_workspace_bytes(batch, max_row_len, k))
+
+
+def topk_transform_raw(scores: torch.Tensor, seq_lens: torch.Tensor, k: int,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact top-k positions of each row of ``scores`` (raw form)."""
+    lib = load_library()
+    batch, row_stride = _scores_2d(scores)
+    dev = scores.device
+    _vector(seq_lens, "seq_lens", batch, dev)
+    out = _out(out, batch, k, dev)
+    with torch.cuda.device(dev):
+        st = lib.topk_transform_raw(scores.data_ptr(), row_stride, seq_lens.data_ptr(), batch, k,
+                                    out.data_ptr(), None, 0, _stream(stream, dev))
+    _check(st, "topk_transform_raw")
+    return out
+
+
+def topk_transform_paged(scores: torch.Tensor, seq_lens: torch.Tensor, page_table: torch.Tensor,
+                         page_size: int, k: int, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Exact top-k of each row, each position j written as
+    page_table[b, j // page_size] * page_size + j % page_size."""
+    lib = load_library()
+    batch, row_stride = _scores_2d(scores)
+    dev = scores.device
+    _vector(seq_lens, "seq_lens", batch, dev)
+    _cuda_tensor(page_table, "page_table", torch.int32, dev)
+    if page_table.dim() != 2 or page_table.shape[0] != batch or (
+            page_table.shape[1] > 1 and page_table.stride(1) != 1):
+        raise ValueError("page_table must be [batch, pages] int32 with unit inner stride")
+    pt_stride = int(page_table.stride(0)) if batch > 1 else int(page_table.shape[1])
+    if pt_stride < max(int(page_table.shape[1]), 1):
+        raise ValueError("page_table rows must not overlap (use .contiguous() on expanded tables)")
+    if page_table.shape[1] * page_size < min(row_stride, scores.shape[1]):
+        raise ValueError("page_table has too few pages for the rows")
+    out = _out(out, batch, k, dev)
+    with torch.cuda.device(dev):
+        st = lib.topk_transform_paged(scores.data_ptr(), row_stride, seq_lens.data_ptr(),
+                                      page_table.data_ptr(), pt_stride, page_size, batch, k,
+                                      out.data_ptr(), None, 0, _stream(stream, dev))
+    _check(st, "topk_transform_paged")
+    return out
+
+
+def topk_transform_ragged(scores: torch.Tensor, row_starts: torch.Tensor, seq_lens: torch.Tensor,
+                          k: int, max_row_len_hint: int = 0, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """Exact top-k of packed rows scores[row_starts[b] : row_starts[b] + seq_lens[b]];
+    each position j is written as row_starts[b] + j."""
+    lib = load_library()
+    _cuda_tensor(scores, "scores", torch.float32)
+    if scores.dim() != 1 or (scores.numel() > 1 and scores.stride(0) != 1):
+        raise ValueError("ragged scores must be a contiguous 1-D fp32 tensor")
+    dev = scores.device
+    batch = int(row_starts.shape[0]) if row_starts.dim() == 1 else -1
+    _vector(row_starts, "row_starts", batch, dev)
+    _vector(seq_lens, "seq_lens", batch, dev)
+    out = _out(out, batch, k, dev)
+    with torch.cuda.device(dev):
+        st = lib.topk_transform_ragged(scores.data_ptr(), row_starts.data_ptr(),
+                                       seq_lens.data_ptr(), int(max_row_len_hint), batch, k,
+                                       out.data_ptr(), None, 0, _stream(stream, dev))
+    _check(st, "topk_transform_ragged")
+    return out
+
+
+def topk_set_row_split(g: int) -> int:
+    """CTAs per row (1, 2, 4, 8, 16); g < 1 restores the built-in choice."""
+    return int(load_library().topk_set_row_split(int(g)))
+
+
+def topk_set_tie_capacity(cap: int) -> int:
+    """Entries of the shared tie buffer (0 .. TOPK_TIE_CAPACITY_MAX); for tests."""
+    return int(load_library().topk_set_tie_capacity(int(cap)))

@@ -1,0 +1,42 @@
+// Internal interface between the C ABI (topk_api.cu) and the kernels
+// (topk_select.cu). Not installed; the public interface is include/topk_transform.h.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace topk_gb300 {
+
+enum Form : int { kRaw = 0, kPaged = 1, kRagged = 2 };
+
+constexpr int kThreads = 512;          // threads per CTA
+constexpr int kMaxBins = 4096;         // widest histogram (12 key bits)
+constexpr int kTieCapMax = 4096;       // shared tie buffer entries, 8 bytes each
+constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
+
+struct Params {
+  const float* scores;
+  int64_t row_stride;          // raw, paged: elements between row starts
+  const int32_t* seq_lens;     // [batch]
+  const int32_t* row_starts;   // ragged: [batch]
+  const int32_t* page_table;   // paged: [batch, pt_stride]
+  int64_t pt_stride;
+  int32_t page_size;
+  int32_t page_shift;          // log2(page_size) when it is a power of two, else -1
+  int32_t* out;                // [batch, k]
+  int32_t k;
+  int32_t tie_cap;             // <= kTieCapMax
+  int32_t batch;
+};
+
+// Dynamic shared memory one CTA needs for a cluster of `g` CTAs.
+size_t smem_bytes(int g, int tie_cap);
+
+// One-time per-device function attributes (max dynamic smem, cluster size 16).
+cudaError_t prepare_device();
+
+// Enqueue the kernel: grid = batch * g CTAs in clusters of g along x.
+cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);
+
+}  // namespace topk_gb300
