@@ -1,0 +1,441 @@
+"""Benchmark of the exact per-row top-k transform on GB300 (one JSON line on stdout).
+
+Workload (the 128k-context decode sweep of the indexer top-k): B=256 rows of
+c4_len=32768 fp32 scores, N(0,1) plus one N(0, sigma=4) offset per row, full
+seq_lens, k=1024, paged output (page_size=64, a random page permutation per row).
+One step is one call of topk_transform_paged over the batch.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from a CUDA graph
+whose nodes cycle through R input sets that together exceed 4x the L2 size, so
+every step reads its scores from HBM; CUDA events on the launching stream bracket
+the K steps, with a device synchronise (and, under torchrun, a barrier) on both
+sides; the slowest rank's time counts. nvidia-smi samples the clocks meanwhile.
+
+Also reported: the roofline of the kernel (algorithmic bytes per launch over its
+average launch time, against the measured HBM copy bandwidth), the end-to-end
+rate through the same public call with pinned host buffers and the copies inside
+the timed region, the CPU oracle's rate on the host cores (a baseline only), and
+a sweep over the other batch sizes and the raw form.
+
+``--impl reference`` times the CPU oracle instead, on the same workload and
+metric; each step processes one row per host core.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "top-k rows/sec & scored Gelem/s at c4_len=32768,k=1024 (1 GB300); % HBM roofline"
+C4_LEN, K_TOP, PAGE_SIZE = 32768, 1024, 64
+KERNEL_NAME = "topk_rows_kernel"
+KERNEL_SRC = os.path.join(ROOT, "sparse_attention_indexer_sm_gb300", "csrc", "topk_select.cu")
+PROFILE = os.path.join(ROOT, "profiles", "topk_rows_kernel_paged_b256_n32768.md")
+L2_FACTOR = 4
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=256)
+    ap.add_argument("--form", choices=["paged", "raw"], default="paged")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_bytes(batch: int, L: int, k: int, form: str, page_size: int = PAGE_SIZE) -> int:
+    """Bytes the method must move per call: scores read once, seq_len, the k output
+    slots, and (paged) one page-table entry per distinct page that can hold a winner."""
+    per_row = 4 * L + 4 + 4 * k
+    if form == "paged":
+        per_row += 4 * min(k, (L + page_size - 1) // page_size)
+    elif form == "ragged":
+        per_row += 4
+    return batch * per_row
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(batch: int, form: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload and the kernel source has not changed since."""
+    if batch != 256 or form != "paged":
+        return None
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            key, _, v = line.strip()[2:].partition(":")
+            vals[key.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != source_sha():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"topk_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t_start: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        mx = [float(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def device_sets(w, n_sets, dev, torch):
+    """n_sets device copies of one workload (distinct buffers, identical bits)."""
+    s_host = torch.from_numpy(w.scores)
+    sets = []
+    for _ in range(n_sets):
+        d = {"scores": s_host.to(dev), "seq": torch.from_numpy(w.seq_lens).to(dev),
+             "out": torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)}
+        if w.form == "paged":
+            d["pt"] = torch.from_numpy(w.page_table).to(dev)
+        sets.append(d)
+    return sets
+
+
+def call(pkg, w, d, stream):
+    if w.form == "paged":
+        pkg.topk_transform_paged(d["scores"], d["seq"], d["pt"], w.page_size, w.k, out=d["out"],
+                                 stream=stream)
+    else:
+        pkg.topk_transform_raw(d["scores"], d["seq"], w.k, out=d["out"], stream=stream)
+
+
+def time_steps(pkg, w, steps, warmup, dev, torch, l2_bytes, dist=None, clocks=None):
+    """Time exactly `steps` calls (CUDA graph replay over rotating input sets).
+    Returns (seconds, launches)."""
+    set_bytes = w.scores.nbytes + w.seq_lens.nbytes + (w.page_table.nbytes if w.form == "paged" else 0)
+    n_sets = max(2, min(4096, math.ceil(L2_FACTOR * l2_bytes / set_bytes)))
+    sets = device_sets(w, n_sets, dev, torch)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):
+            call(pkg, w, sets[i % n_sets], stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for d in sets:
+                call(pkg, w, d, stream)
+        graph.replay()  # one untimed replay
+        stream.synchronize()
+    full, rest = divmod(steps, n_sets)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graph.replay()
+        for i in range(rest):
+            call(pkg, w, sets[i], stream)
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    secs = start.elapsed_time(end) / 1e3
+    del graph, sets
+    torch.cuda.empty_cache()
+    return secs, steps, (t0, t1), n_sets
+
+
+def time_e2e(pkg, w, steps, dev, torch):
+    """Same call with pinned host inputs: H2D of scores/seq_lens/page_table, the
+    kernel, D2H of the result, every step, inside the timed region."""
+    stream = torch.cuda.Stream(dev)
+    h_scores = torch.from_numpy(w.scores).pin_memory()
+    h_seq = torch.from_numpy(w.seq_lens).pin_memory()
+    h_pt = torch.from_numpy(w.page_table).pin_memory() if w.form == "paged" else None
+    h_out = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
+    d = {"scores": torch.empty_like(h_scores, device=dev), "seq": torch.empty_like(h_seq, device=dev),
+         "out": torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)}
+    if h_pt is not None:
+        d["pt"] = torch.empty_like(h_pt, device=dev)
+
+    def step():
+        d["scores"].copy_(h_scores, non_blocking=True)
+        d["seq"].copy_(h_seq, non_blocking=True)
+        if h_pt is not None:
+            d["pt"].copy_(h_pt, non_blocking=True)
+        call(pkg, w, d, stream)
+        h_out.copy_(d["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        end.synchronize()
+    secs = start.elapsed_time(end) / 1e3
+    h2d = h_scores.numel() * 4 + h_seq.numel() * 4 + (h_pt.numel() * 4 if h_pt is not None else 0)
+    d2h = h_out.numel() * 4
+    return secs, h2d, d2h
+
+
+def cpu_baseline(w, seconds: float = 1.5):
+    """The oracle as it stands, on every host core, over whole batches of the same
+    workload until about `seconds` of wall time (a bounded sample)."""
+    import oracle
+    o = oracle.default()
+    cores = o.usable_cores()
+    rows, t0 = 0, time.perf_counter()
+    while True:
+        o.run(w, threads=cores)
+        rows += w.batch
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": rows / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} rows ({rows // w.batch} full batches of the bench workload), "
+                      f"{el:.2f} s wall on {cores} threads"}
+
+
+def workload_for(batch: int, form: str):
+    return workloads.config3(batch, form)
+
+
+def describe(w) -> str:
+    return (f"topk_transform_{w.form} B={w.batch} c4_len={C4_LEN} k={w.k}"
+            + (f" page_size={w.page_size}" if w.form == "paged" else "")
+            + " decode scores N(0,1)+N(0,4) row offset, full seq_lens")
+
+
+def run_ours(args):
+    import torch
+    import sparse_attention_indexer_sm_gb300 as pkg
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = td
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkg.load_library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    peak, peak_kind = peaks()
+
+    w = workload_for(args.batch, args.form)
+    with ClockSampler(local) as clk:
+        secs, launches, (t0, t1), n_sets = time_steps(pkg, w, args.steps, args.warmup, dev, torch,
+                                                      l2, dist)
+        clocks = clk.summary(t0, t1)
+    if dist is not None:
+        t = torch.tensor([secs], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    per_call = secs / args.steps
+    rows_per_s = world * w.batch * args.steps / secs
+    gelem = world * w.scored_elements * args.steps / secs / 1e9
+    alg = algorithmic_bytes(w.batch, C4_LEN, w.k, w.form)
+    achieved = alg / per_call / 1e9
+    traffic = profiled_traffic(w.batch, w.form)
+
+    e2e_steps = max(20, min(args.steps, 400))
+    e_secs, h2d, d2h = time_e2e(pkg, w, e2e_steps, dev, torch)
+
+    result = {
+        "metric": METRIC,
+        "value": rows_per_s,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": per_call * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "batch_per_gpu": w.batch, "c4_len": C4_LEN,
+                   "k": w.k, "form": w.form, "page_size": w.page_size,
+                   "l2": f"inputs larger than L2: {n_sets} rotating input sets, "
+                         f"{n_sets * w.scores.nbytes / 1e6:.0f} MB >= {L2_FACTOR}x L2 ({l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph replay, CUDA events on the launching stream",
+                   "parallelism": f"rows sharded, {world} GPU(s), no collective"},
+        "scored_gelem_per_s": gelem,
+        "us_per_call": per_call * 1e6,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                     "frac_of_nominal_8TBps": achieved / 8000.0, "kernel": KERNEL_NAME},
+        "e2e": {"value": world * w.batch * e2e_steps / e_secs, "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e_secs / e2e_steps * 1e3},
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0 and world == 1 and not args.no_sweep:
+        sweep = []
+        for (b, form) in ((1, "paged"), (8, "paged"), (64, "paged"), (128, "paged"),
+                          (256, "paged"), (256, "raw"), (64, "raw")):
+            if (b, form) == (w.batch, w.form):
+                continue
+            ws = workload_for(b, form)
+            steps = 20000 if b >= 64 else 40000
+            s, _, _, ns = time_steps(pkg, ws, steps, 20, dev, torch, l2)
+            pc = s / steps
+            ab = algorithmic_bytes(b, C4_LEN, ws.k, form)
+            sweep.append({"batch": b, "form": form, "us_per_call": pc * 1e6,
+                          "rows_per_s": b / pc, "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
+                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+        result["sweep"] = sweep
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    o = oracle.default()
+    cores = o.usable_cores()
+    w = workload_for(args.batch, args.form)
+    # one step: `cores` rows of the workload, one per host core
+    rows_per_step = min(cores, w.batch)
+    sub = workloads.Workload(w.name, w.form, w.k, w.scores[:rows_per_step],
+                             w.seq_lens[:rows_per_step],
+                             None if w.page_table is None else w.page_table[:rows_per_step],
+                             w.page_size)
+    for _ in range(args.warmup):
+        o.run(sub, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.run(sub, threads=cores)
+    secs = time.perf_counter() - t0
+    value = rows_per_step * args.steps / secs
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "batch_per_gpu": w.batch, "c4_len": C4_LEN, "k": w.k,
+                   "form": w.form, "page_size": w.page_size},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {rows_per_step} rows of the workload, one per core"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI (needs a GB300).
+
+Every comparison is bit-exact: each output row, taken as a set of int32 slots,
+must equal the oracle's, and the un-mapped selection must pass the complete
+invariant check of tests/checks.py. Inputs come from workloads.py (seeded, on
+the host) and are copied to the device unchanged.
+"""
+
+from __future__ import annotations
+
+import contextlib
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from checks import check_workload, same_sets
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_indexer_sm_gb300 as p
+    p.load_library()
+    return p
+
+
+@contextlib.contextmanager
+def settings(pkg, split=None, tie_cap=None):
+    prev_split = pkg.topk_set_row_split(split) if split is not None else None
+    prev_cap = pkg.topk_set_tie_capacity(tie_cap) if tie_cap is not None else None
+    try:
+        yield
+    finally:
+        if split is not None:
+            pkg.topk_set_row_split(prev_split)
+        if tie_cap is not None:
+            pkg.topk_set_tie_capacity(prev_cap)
+
+
+def run_gpu(pkg, w, stream=None) -> np.ndarray:
+    dev = torch.device("cuda:0")
+    scores = torch.from_numpy(np.ascontiguousarray(w.scores)).to(dev)
+    seq = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(dev)
+    out = torch.full((w.batch, w.k), -7, dtype=torch.int32, device=dev)  # poison
+    if w.form == "raw":
+        pkg.topk_transform_raw(scores, seq, w.k, out=out, stream=stream)
+    elif w.form == "paged":
+        pt = torch.from_numpy(np.ascontiguousarray(w.page_table)).to(dev)
+        pkg.topk_transform_paged(scores, seq, pt, w.page_size, w.k, out=out, stream=stream)
+    else:
+        rs = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
+        hint = int(np.max(w.seq_lens, initial=0))
+        pkg.topk_transform_ragged(scores, rs, seq, w.k, max_row_len_hint=hint, out=out,
+                                  stream=stream)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def assert_parity(w, got, check_rows=None):
+    exp = oracle.run(w)
+    ok = same_sets(got, exp)
+    if not ok.all():
+        b = int(np.flatnonzero(~ok)[0])
+        diff = np.setxor1d(got[b], exp[b])
+        raise AssertionError(f"{w.name}: {int((~ok).sum())} rows differ from the oracle; "
+                             f"row {b} symmetric difference {diff[:10].tolist()}")
+    errs = check_workload(w, got, max_rows=check_rows)
+    assert not errs, f"{w.name}: {errs[:3]}"
+
+
+# ------------------------------------------------------------ the pages' workloads
+
+def test_config1_unit_shape(pkg):
+    w = workloads.config1()
+    assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("bs", [1, 48])
+@pytest.mark.parametrize("c4_len", [2048, 8192, 32768])
+def test_unit_test_shapes(pkg, bs, c4_len):
+    """The parameter grid of test_deepseek_v4_topk_transform (PR #36004 page)."""
+    w = workloads.unit_test_shape(bs, c4_len)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("c4_len", [8192, 32768])
+def test_config2_random_lengths(pkg, c4_len):
+    w = workloads.config2(c4_len)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("form", ["raw", "paged"])
+@pytest.mark.parametrize("batch", [1, 8, 64, 128, 256])
+def test_config3_decode_sweep(pkg, batch, form):
+    w = workloads.config3(batch, form)
+    assert_parity(w, run_gpu(pkg, w), check_rows=16)
+
+
+@pytest.mark.parametrize("dist", ["banded", "narrow", "subnormal"])
+def test_config4_adversarial_ragged(pkg, dist):
+    w = workloads.config4(dist)
+    assert_parity(w, run_gpu(pkg, w), check_rows=4)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4])
+def test_config5_long_rows(pkg, batch):
+    w = workloads.config5(batch)
+    assert_parity(w, run_gpu(pkg, w), check_rows=2)
+
+
+# ------------------------------------------------------------ every execution path
+
+def _mixed(seed, dist, batch=6, stride=20000, k=1024, dup=True, form="paged"):
+    g = workloads.rng(seed)
+    scores = workloads.random_rows(g, batch, stride, dist, dup)
+    seq = g.integers(k // 2, stride + 5, size=batch).astype(np.int32)
+    pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, 64))
+    w = workloads.Workload(f"{dist}_{form}_s{seed}", form, k, scores, seq, pt, 64)
+    return w
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("dist", ["normal", "decode", "banded", "narrow", "subnormal", "heavy_tail"])
+def test_every_row_split(pkg, split, dist):
+    """Single-CTA and cluster row-split paths give the oracle's set (cross-path A/B
+    of the PR #36004 page's index-set comparison, restated per split)."""
+    w = _mixed(100 + split, dist)
+    with settings(pkg, split=split):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("tie_cap", [0, 1, 16, 300, 4096])
+@pytest.mark.parametrize("split", [1, 4])
+@pytest.mark.parametrize("dist", ["decode", "banded", "narrow", "subnormal"])
+def test_tie_buffer_capacity(pkg, tie_cap, split, dist):
+    """Small tie buffers force more radix rounds and the position-ordered rescan."""
+    w = _mixed(200 + tie_cap, dist, k=2048)
+    with settings(pkg, split=split, tie_cap=tie_cap):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("split", [1, 2, 16])
+def test_all_equal_rows(pkg, split):
+    """Every key ties: the first k positions win."""
+    batch, stride, k = 3, 50000, 2048
+    scores = np.full((batch, stride), 1.5, np.float32)
+    scores[1, ::7] = -0.0
+    scores[2] = 0.0
+    seq = np.array([stride, stride - 3, 40001], np.int32)
+    w = workloads.Workload("all_equal", "raw", k, scores, seq)
+    with settings(pkg, split=split):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("k", [1, 2, 7, 100, 1000, 1024, 1025, 2047, 2048])
+def test_any_k(pkg, k):
+    w = _mixed(300 + k, "decode", batch=4, stride=9000, k=k, form="raw")
+    assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("stride", [1, 2, 3, 5, 1023, 1024, 1025, 4097, 8191])
+def test_odd_row_strides_and_short_rows(pkg, stride):
+    """Row starts at every 4-byte alignment; L around k; L = 0; L > stride."""
+    g = workloads.rng(400 + stride)
+    k = 1024
+    batch = 12
+    scores = workloads.random_rows(g, batch, stride, "normal", dup=True)
+    seq = np.array([0, 1, stride, stride + 9, -5, min(k, stride), min(k + 1, stride),
+                    stride // 2, max(stride - 1, 0), 2 * stride, 3, stride], np.int32)
+    for form in ("raw", "paged"):
+        pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, 64))
+        w = workloads.Workload(f"stride{stride}_{form}", form, k, scores, seq, pt, 64)
+        assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 16, 48, 64, 100, 4096])
+def test_page_sizes(pkg, page_size):
+    g = workloads.rng(500 + page_size)
+    batch, stride, k = 4, 12000, 1024
+    scores = workloads.random_rows(g, batch, stride, "heavy_tail")
+    seq = np.array([stride, 5000, 800, 11999], np.int32)
+    pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, page_size))
+    w = workloads.Workload(f"ps{page_size}", "paged", k, scores, seq, pt, page_size)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+def test_identity_page_table_equals_raw(pkg):
+    w = workloads.unit_test_shape(48, 32768)
+    paged = run_gpu(pkg, w)
+    raw = run_gpu(pkg, w.as_raw())
+    assert same_sets(paged, raw).all()
+
+
+@pytest.mark.parametrize("split", [1, 4, 16])
+def test_ragged_odd_offsets_and_empty_rows(pkg, split):
+    g = workloads.rng(600 + split)
+    lens = np.array([0, 1, 2047, 2048, 2049, 70001, 3, 150000, 0, 65536], np.int64)
+    gaps = g.integers(0, 7, size=lens.shape[0])
+    starts = (np.concatenate([[0], np.cumsum(lens + gaps)[:-1]]) + 1).astype(np.int32)
+    total = int(starts[-1] + lens[-1] + 5)
+    scores = workloads.row_values(g, "banded", total, dup=True)
+    w = workloads.Workload("ragged_edges", "ragged", 2048, scores, lens.astype(np.int32),
+                           None, 64, starts)
+    with settings(pkg, split=split):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+def test_nan_keys_follow_the_key_order(pkg):
+    """NaN bit patterns are ranked by their key like any other (+NaN above +inf)."""
+    g = workloads.rng(700)
+    scores = workloads.random_rows(g, 2, 5000, "normal")
+    scores[0, ::97] = np.float32(np.nan)
+    scores[1, ::89] = -np.float32(np.nan)
+    seq = np.array([5000, 5000], np.int32)
+    w = workloads.Workload("nan", "raw", 1024, scores, seq)
+    got = run_gpu(pkg, w)
+    assert same_sets(got, oracle.run(w)).all()
+
+
+def test_empty_batch(pkg):
+    dev = torch.device("cuda:0")
+    out = pkg.topk_transform_raw(torch.zeros((0, 16), device=dev),
+                                 torch.zeros(0, dtype=torch.int32, device=dev), 4)
+    assert out.shape == (0, 4)
+
+
+def test_invalid_k_raises(pkg):
+    dev = torch.device("cuda:0")
+    s = torch.zeros((1, 16), device=dev)
+    L = torch.full((1,), 16, dtype=torch.int32, device=dev)
+    for k in (0, pkg.TOPK_MAX_K + 1):
+        with pytest.raises(pkg.TopkError, match="unsupported k"):
+            pkg.topk_transform_raw(s, L, k)
+
+
+def test_side_stream_and_repeatability(pkg):
+    w = workloads.config3(64, "paged")
+    s = torch.cuda.Stream()
+    a = run_gpu(pkg, w, stream=s)
+    b = run_gpu(pkg, w)
+    assert (np.sort(a, 1) == np.sort(b, 1)).all()
+    assert_parity(w, a, check_rows=4)

@@ -113,8 +113,7 @@ def row_values(g: np.random.Generator, dist: str, n: int, dup: bool = False) -> 
 # ---------------------------------------------------------------- layout helpers
 
 def identity_page_table(batch: int, n_pages: int) -> np.ndarray:
-    return np.ascontiguousarray(
-        np.broadcast_to(np.arange(n_pages, dtype=np.int32), (batch, n_pages)))
+    return np.tile(np.arange(n_pages, dtype=np.int32), (batch, 1))
 
 
 def permuted_page_table(g: np.random.Generator, batch: int, n_pages: int) -> np.ndarray:
