@@ -173,6 +173,20 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- our arm
 
+def max_over_ranks(secs: float, dist, device) -> float:
+    """The slowest rank's time (rows shard across ranks with no data exchange;
+    this timing reduction is the only collective)."""
+    import torch
+    t = torch.tensor([secs], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(batch: int, form: str, rank: int):
+    """Rank r's own rows: the same shapes, its own seed (weak scaling)."""
+    return workloads.config3(batch, form, seed=workloads.BASE_SEED + 2 + 1000 * rank)
+
+
 def device_sets(w, n_sets, dev, torch):
     """n_sets device copies of one workload (distinct buffers, identical bits)."""
     s_host = torch.from_numpy(w.scores)
@@ -318,15 +332,13 @@ def run_ours(args):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     peak, peak_kind = peaks()
 
-    w = workload_for(args.batch, args.form)
+    w = rank_workload(args.batch, args.form, rank)
     with ClockSampler(local) as clk:
         secs, launches, (t0, t1), n_sets = time_steps(pkg, w, args.steps, args.warmup, dev, torch,
                                                       l2, dist)
         clocks = clk.summary(t0, t1)
     if dist is not None:
-        t = torch.tensor([secs], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+        secs = max_over_ranks(secs, dist, dev)
     per_call = secs / args.steps
     rows_per_s = world * w.batch * args.steps / secs
     gelem = world * w.scored_elements * args.steps / secs / 1e9

@@ -120,12 +120,18 @@ int topk_last_cuda_error(void);
  * row_split, restated for a cluster). The environment variable TOPK_ROW_SPLIT
  * sets the initial value.
  *
- * topk_set_tie_capacity(cap): entries of the shared tie buffer, clamped to
- * [0, TOPK_TIE_CAPACITY_MAX]. Smaller values force the exact position-ordered
- * rescan for more rows (used by tests); the result never changes. */
+ * topk_set_tie_capacity(cap): entries of the shared candidate/tie buffer,
+ * clamped to [0, TOPK_TIE_CAPACITY_MAX]. Smaller values send more rows through
+ * the exact tier's extra radix rounds and its position-ordered rescan (used by
+ * tests); the result never changes.
+ *
+ * topk_set_fast_tier(enable): 1 (default) first tries the one-pass filter whose
+ * threshold comes from a sample of the row and is verified afterwards; 0 always
+ * runs the exact histogram tier. The result is the same either way. */
 #define TOPK_TIE_CAPACITY_MAX 4096
 int topk_set_row_split(int g);
 int topk_set_tie_capacity(int cap);
+int topk_set_fast_tier(int enable);
 
 #ifdef __cplusplus
 } /* extern "C" */

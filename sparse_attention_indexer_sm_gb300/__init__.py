@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
     "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged",
-    "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity",
+    "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
 TOPK_MAX_K = 2048
@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_set_row_split.argtypes = [ctypes.c_int]
             lib.topk_set_tie_capacity.restype = ctypes.c_int
             lib.topk_set_tie_capacity.argtypes = [ctypes.c_int]
+            lib.topk_set_fast_tier.restype = ctypes.c_int
+            lib.topk_set_fast_tier.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -202,3 +204,8 @@ def topk_set_row_split(g: int) -> int:
 def topk_set_tie_capacity(cap: int) -> int:
     """Entries of the shared tie buffer (0 .. TOPK_TIE_CAPACITY_MAX); for tests."""
     return int(load_library().topk_set_tie_capacity(int(cap)))
+
+
+def topk_set_fast_tier(enable: bool) -> int:
+    """1: try the sampled-threshold one-pass filter first (default); 0: exact tier only."""
+    return int(load_library().topk_set_fast_tier(1 if enable else 0))

@@ -20,6 +20,7 @@ constexpr int kRowSplitUnset = INT_MIN;
 
 std::atomic<int> g_row_split{kRowSplitUnset};
 std::atomic<int> g_tie_cap{topk_gb300::kTieCapMax};
+std::atomic<int> g_fast_tier{1};
 thread_local int t_last_cuda_error = 0;
 
 struct DeviceState {
@@ -82,6 +83,7 @@ int run(Form form, Params p, int64_t row_len_hint, cudaStream_t stream) {
   const int g = choose_split(p.batch, row_len_hint, ds.sm_count);
   if (static_cast<int64_t>(p.batch) * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
   p.tie_cap = g_tie_cap.load(std::memory_order_relaxed);
+  p.use_filter = g_fast_tier.load(std::memory_order_relaxed);
   e = topk_gb300::launch(form, p, g, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return TOPK_OK;
@@ -175,6 +177,10 @@ int topk_set_row_split(int g) {
   const int prev = row_split_setting();
   g_row_split.store(g < 1 ? 0 : g, std::memory_order_relaxed);
   return prev < 1 ? 0 : prev;
+}
+
+int topk_set_fast_tier(int enable) {
+  return g_fast_tier.exchange(enable != 0 ? 1 : 0, std::memory_order_relaxed);
 }
 
 int topk_set_tie_capacity(int cap) {

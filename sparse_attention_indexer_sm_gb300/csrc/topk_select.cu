@@ -1,40 +1,56 @@
 // Exact per-row top-k selection of fp32 indexer scores on GB300 (sm_103a).
 //
 // One thread-block cluster of G CTAs (G = 1, 2, 4, 8 or 16) owns one row; each
-// CTA owns a contiguous slice of it. The steps follow the exact "coop" top-k of
-// the sglang PR #37591 summary page (section "实现拆解" (implementation
-// breakdown) item 1 and the coop_topk_kernel excerpt under "关键源码片段"),
-// re-planned for this machine:
+// CTA owns a contiguous slice of it. The method is the exact "coop" top-k of the
+// sglang PR #37591 summary page (section "实现拆解" (implementation breakdown)
+// item 1 and the coop_topk_kernel excerpt under "关键源码片段"): an
+// order-preserving 32-bit key, radix histograms over the high key bits to find
+// the threshold bucket, a scatter of winners and threshold-bucket ties, an exact
+// refinement of the ties on the full key, and a rescan when the tie buffer
+// overflows. On this machine it runs in two tiers:
 //
-//  1. key      every fp32 becomes its order-preserving 32-bit key (negatives
-//              bit-inverted, the rest with the sign bit set: unsigned order ==
-//              float order; PR #37591 page, order_key32).
-//  2. round 0  a 4096-bin shared-memory histogram of the top 12 key bits over the
-//              slice, read from HBM with 128-bit loads. With G > 1 the slices'
-//              histograms are summed into CTA 0 through distributed shared
-//              memory; CTA 0 finds the threshold bin with a block-wide suffix
-//              scan and sends it back (the page's "binary search for the threshold
-//              bucket" computes the same bin).
-//  3. more     while the threshold bin holds more elements than the tie buffer,
-//     rounds   one more histogram of the next 12 (then 8) key bits restricted to
-//              that bin narrows it (the page's second, 4-bit round does the same
-//              job; this build uses wider rounds so that fewer passes are needed
-//              when values concentrate).
-//  4. scatter  elements above the threshold bin are winners and go straight to the
-//              output, mapped; elements in it go to the shared tie buffer of CTA 0
-//              (the page's "scatter pass"). Both use one shared atomic per warp.
-//  5. refine   CTA 0 selects the missing winners among the ties by radix rounds on
-//              the 64-bit composite (key, ~position): the rest of the key first,
-//              then the position, so equal keys go to the smaller position (the
-//              page's "radix sort of the ties on the full fp32 key").
-//  6. rescan   when even the full 32-bit key leaves more equal elements than the
-//              tie buffer holds (88% identical values, say), no element is
-//              dropped: every CTA re-reads its slice in position order and takes
-//              its quota of the equal elements by a block-wide prefix count (the
-//              page's "overflow rescan of the whole row").
+// Fast tier (one pass over the row, normally the only one):
+//  F1. sample    each CTA loads a strided sample of its slice (one 16-byte quad
+//                in every `stride` >= 8) before anything else. Two sample ranks are
+//                wanted: r_s, a few standard deviations below the expected sample rank
+//                of the row's k-th key, and r_lo as far above it. A 4096-bin histogram
+//                of the top 12 key bits (summed over the cluster through distributed
+//                shared memory) finds the coarse bins of both; a second 4096-bin
+//                histogram spanning just those coarse bins resolves them: lambda is the
+//                lower edge of r_s's fine bin, lambda_hi the upper edge of r_lo's. Rows
+//                that fit the candidate buffer skip the sample (lambda = 0).
+//  F2. filter    one streaming pass with 128-bit loads compares every raw fp32 bit
+//                pattern with lambda (a single integer compare: for lambda in the
+//                non-negative range a signed compare, otherwise an unsigned one,
+//                both equal to "key >= lambda"); candidates go, as (key, position),
+//                to CTA 0's shared buffer and into CTA 0's candidate histogram, whose
+//                4096 bins of width 2^s2 start at lambda (s2 chosen so that about
+//                2048 bins span [lambda, lambda_hi]; the last bin takes every larger
+//                key).
+//  F3. select    if the cluster found between k and capacity candidates, every
+//                element of the exact top-k is among them (they hold k elements with
+//                key >= lambda, so the k-th key is >= lambda). CTA 0 finds the
+//                threshold bin of the candidate histogram, writes the candidates above
+//                it, and orders the few candidates of that bin on the 64-bit composite
+//                (key, ~position), so equal keys go to the smaller position. Otherwise
+//                the exact tier runs.
 //
-// No step waits on another CTA except through the hardware cluster barrier, so
-// there is no spin loop, no global workspace and no inter-launch dependency.
+// Exact tier (any distribution; the page's design, re-planned):
+//  E1. rounds    4096-bin shared histograms of the top 12 key bits over the slice
+//                (merged over the cluster), then of the next 12 and 8 bits inside
+//                the threshold bin while that bin holds more elements than the tie
+//                buffer (the page's round0/round1 coarse histograms).
+//  E2. scatter   elements above the threshold bin go straight to the output;
+//                elements in it go to CTA 0's tie buffer (the page's scatter pass).
+//  E3. refine    as F3, on the ties (the page's radix sort of the ties on the full
+//                fp32 key).
+//  E4. rescan    when more elements than the buffer holds equal the exact 32-bit
+//                threshold key, every CTA re-reads its slice in position order and
+//                takes its quota of equal elements by a block-wide prefix count (the
+//                page's overflow rescan): nothing is ever dropped.
+//
+// No step waits on another CTA except through the hardware cluster barrier: no
+// spin loop, no global workspace, one launch per call.
 
 #include <cstdint>
 
@@ -44,17 +60,38 @@ namespace topk_gb300 {
 namespace {
 
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;            // 128-bit loads in flight per thread per step
-constexpr int kRowRoundBits = 12;     // histogram width of the passes over the row
-constexpr int kBufRoundBits = 10;     // histogram width of the rounds over the ties
+constexpr int kUnroll = 4;            // 128-bit loads in flight per thread per step (exact tier)
+constexpr int kFilterUnroll = 8;      // 128-bit loads in flight per thread in the filter
+constexpr int kRowRoundBits = 12;     // histogram width of the rounds over the row
+constexpr int kBufRoundBits = 12;     // histogram width of the rounds over a buffer
+constexpr int kSampleQuads = 2;       // sampled 16-byte quads per thread
+constexpr uint32_t kPrefetchBytes = 16384;  // one bulk L2 prefetch
+constexpr int kPtCap = 4096;          // page-table entries staged in shared memory
+constexpr int kRankDirect = 64;       // threshold bins this small are ordered by rank count
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Histograms are stored padded, one spare word after every 32 bins, so that the
+// threshold scan (each thread reads a run of consecutive bins) is free of shared
+// memory bank conflicts.
+__host__ __device__ constexpr int hist_index(int b) { return b + (b >> 5); }
+constexpr int kHistWords = hist_index(kMaxBins);
+constexpr int kListCap = kHistWords / 2;  // (key, position) entries of the list region
 
 struct Ctl {
   uint32_t scan[kWarps];              // per-warp partials of block scans
   uint32_t sel_t, sel_above, sel_count;  // threshold bin of the current round
   uint32_t win_cnt, tie_cnt, out_cnt;    // slot counters
+  uint32_t cand_cnt;                  // candidates found by the filter (CTA 0)
+  uint32_t n_cand;                    // cand_cnt of CTA 0, broadcast
+  uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
+  uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
+  uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
   uint32_t xt[kMaxCluster];           // per-CTA threshold-bin elements
+};
+
+struct Sel {
+  uint32_t t, above, count;
 };
 
 // ------------------------------------------------------------------ primitives
@@ -74,6 +111,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t r;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
   return r;
 }
 
@@ -99,6 +142,13 @@ __device__ __forceinline__ void dsmem_add(uint32_t addr, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t dsmem_fetch_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
@@ -108,19 +158,23 @@ __device__ __forceinline__ void dsmem_st2(uint32_t addr, uint32_t a, uint32_t b)
                : "memory");
 }
 
-// 128-bit read-only load that does not allocate in L1 (each byte is read once
-// per pass; a second pass finds it in L2).
+// 128-bit read-only load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
   return v;
 }
 
-// Reserve n consecutive slots of *counter for this lane; one atomic per warp.
-// Must be called by all 32 lanes.
-__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t n) {
+// Ask the memory system to bring [p, p + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16). Nothing waits for it; later loads simply hit L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// Inclusive warp prefix sum of n; *total gets the warp sum. All 32 lanes.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t n, uint32_t* total) {
   const int lane = threadIdx.x & 31;
   uint32_t x = n;
 #pragma unroll
@@ -128,13 +182,35 @@ __device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t n) 
     const uint32_t y = __shfl_up_sync(kFull, x, off);
     if (lane >= off) x += y;
   }
-  const uint32_t total = __shfl_sync(kFull, x, 31);
+  *total = __shfl_sync(kFull, x, 31);
+  return x;
+}
+
+// Reserve n consecutive slots of a shared counter for this lane, one atomic per
+// warp. `remote` selects a distributed-shared-memory counter (cluster address).
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t counter_remote,
+                                                 bool remote, uint32_t n) {
+  uint32_t total;
+  const uint32_t x = warp_incl_scan(n, &total);
   uint32_t base = 0;
   if (total != 0) {
-    if (lane == 31) base = atomicAdd(counter, total);
+    if ((threadIdx.x & 31) == 31)
+      base = remote ? dsmem_fetch_add(counter_remote, total) : atomicAdd(counter, total);
     base = __shfl_sync(kFull, base, 31);
   }
   return base + x - n;
+}
+
+// One slot of a local shared counter for each lane whose `pred` holds. All lanes.
+__device__ __forceinline__ uint32_t warp_reserve_bit(uint32_t* counter, bool pred) {
+  const uint32_t b = __ballot_sync(kFull, pred);
+  uint32_t base = 0;
+  if (b != 0) {
+    const int leader = __ffs(b) - 1;
+    if ((threadIdx.x & 31) == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(b)));
+    base = __shfl_sync(kFull, base, leader);
+  }
+  return base + static_cast<uint32_t>(__popc(b & lanemask_lt()));
 }
 
 // Sum over the block; every thread gets the total.
@@ -154,12 +230,8 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, Ctl& ctl) {
 // Exclusive prefix sum in thread order; *total gets the block sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, x, off);
-    if (lane >= off) x += y;
-  }
+  uint32_t wsum;
+  const uint32_t x = warp_incl_scan(v, &wsum);
   if (lane == 31) ctl.scan[warp] = x;
   __syncthreads();
   uint32_t below = 0, all = 0;
@@ -174,17 +246,22 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32
   return below + x - v;
 }
 
-// Threshold bin of histogram h[0, nbins): the bin t where the count from the top
-// reaches `need` (need <= sum of h). Writes t, the count strictly above t and
-// h[t] into ctl.sel_*; all threads see them on return.
+// Threshold bin of the (padded) histogram h of nbins bins: the bin t where the
+// count from the top reaches `need` (need <= sum of h). Writes t, the count
+// strictly above t and h[t] into ctl.sel_*; all threads see them on return.
 __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uint32_t need,
                                                Ctl& ctl) {
+  constexpr int kMaxPer = kMaxBins / kThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = nbins >= kThreads ? nbins / kThreads : 1;
   const int b0 = tid * per;
+  uint32_t c[kMaxPer];
   uint32_t s = 0;
-  if (b0 < nbins)
-    for (int i = 0; i < per; ++i) s += h[b0 + i];
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    c[i] = (i < per && b0 + i < nbins) ? h[hist_index(b0 + i)] : 0u;
+    s += c[i];
+  }
   // suffix scan: thread t gets the count held by threads > t (higher bins)
   uint32_t x = s;
 #pragma unroll
@@ -200,18 +277,103 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
   const uint32_t excl = higher + x - s;
   if (s != 0 && excl < need && need <= excl + s) {
     uint32_t acc = excl;
-    for (int i = per - 1; i >= 0; --i) {
-      const uint32_t c = h[b0 + i];
-      if (acc + c >= need) {
+    bool found = false;
+#pragma unroll
+    for (int i = kMaxPer - 1; i >= 0; --i) {
+      if (!found && i < per && acc + c[i] >= need) {
         ctl.sel_t = static_cast<uint32_t>(b0 + i);
         ctl.sel_above = acc;
-        ctl.sel_count = c;
-        break;
+        ctl.sel_count = c[i];
+        found = true;
       }
-      acc += c;
+      acc += found ? 0u : c[i];
     }
   }
   __syncthreads();
+}
+
+// Two thresholds of one histogram in one scan: need1 -> ctl.sel_*, need2 ->
+// ctl.sel2_* (both need <= sum of h).
+__device__ __forceinline__ void find_threshold2(const uint32_t* h, int nbins, uint32_t need1,
+                                                uint32_t need2, Ctl& ctl) {
+  constexpr int kMaxPer = kMaxBins / kThreads;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nbins >= kThreads ? nbins / kThreads : 1;
+  const int b0 = tid * per;
+  uint32_t c[kMaxPer];
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    c[i] = (i < per && b0 + i < nbins) ? h[hist_index(b0 + i)] : 0u;
+    s += c[i];
+  }
+  uint32_t x = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_down_sync(kFull, x, off);
+    if (lane + off < 32) x += y;
+  }
+  if (lane == 0) ctl.scan[warp] = x;
+  __syncthreads();
+  uint32_t higher = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) higher += w > warp ? ctl.scan[w] : 0u;
+  const uint32_t excl = higher + x - s;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t need = q == 0 ? need1 : need2;
+    if (s != 0 && excl < need && need <= excl + s) {
+      uint32_t acc = excl;
+      bool found = false;
+#pragma unroll
+      for (int i = kMaxPer - 1; i >= 0; --i) {
+        if (!found && i < per && acc + c[i] >= need) {
+          if (q == 0) {
+            ctl.sel_t = static_cast<uint32_t>(b0 + i);
+            ctl.sel_above = acc;
+            ctl.sel_count = c[i];
+          } else {
+            ctl.sel2_t = static_cast<uint32_t>(b0 + i);
+            ctl.sel2_above = acc;
+            ctl.sel2_count = c[i];
+          }
+          found = true;
+        }
+        acc += found ? 0u : c[i];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Cluster-wide threshold bin of the CTAs' histograms `hist` (complete and
+// visible to the whole CTA on entry). With G > 1 the histograms are summed into
+// CTA 0's `mhist` through distributed shared memory; CTA 0 finds the bin, sends
+// it to every CTA and clears `mhist` for the next round.
+__device__ __forceinline__ Sel threshold_of(const uint32_t* hist, uint32_t* mhist, int nbins,
+                                            uint32_t need, int G, int rank, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  if (G == 1) {
+    find_threshold(hist, nbins, need, ctl);
+    return Sel{ctl.sel_t, ctl.sel_above, ctl.sel_count};
+  }
+  const uint32_t m0 = map_rank(smem_addr(mhist), 0);
+  for (int i = tid; i < hist_index(nbins); i += kThreads) {
+    const uint32_t v = hist[i];
+    if (v != 0) dsmem_add(m0 + 4u * static_cast<uint32_t>(i), v);
+  }
+  cluster_sync();
+  if (rank == 0) {
+    find_threshold(mhist, nbins, need, ctl);
+    if (tid > 0 && tid < G) {
+      dsmem_st(map_rank(smem_addr(&ctl.sel_t), tid), ctl.sel_t);
+      dsmem_st(map_rank(smem_addr(&ctl.sel_above), tid), ctl.sel_above);
+      dsmem_st(map_rank(smem_addr(&ctl.sel_count), tid), ctl.sel_count);
+    }
+    for (int i = tid; i < hist_index(nbins); i += kThreads) mhist[i] = 0;
+  }
+  cluster_sync();
+  return Sel{ctl.sel_t, ctl.sel_above, ctl.sel_count};
 }
 
 // ------------------------------------------------------------------ row slices
@@ -220,13 +382,20 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
 // evenly over the cluster, plus the unaligned head (CTA 0) and tail (last CTA).
 struct Slice {
   const float* row;
-  const uint4* vec;       // quad 0 of the aligned body
-  int64_t q0, q1;         // this CTA's quads
-  int32_t vec0;           // row position of quad 0
+  const uint4* vec;       // this CTA's first quad
+  int32_t nq;             // this CTA's quads
+  int32_t j0;             // row position of this CTA's first quad
+  int32_t nvec;           // quads of the whole aligned body
   int32_t n_head;         // positions [0, n_head) belong to this CTA
   int32_t tail0, n_tail;  // positions [tail0, tail0 + n_tail) belong to this CTA
   int32_t lo, hi;         // the CTA's positions as one range [lo, hi)
 };
+
+__device__ __forceinline__ void quad_range(int32_t nvec, int rank, int G, int32_t* q0,
+                                           int32_t* q1) {
+  *q0 = static_cast<int32_t>(static_cast<int64_t>(nvec) * rank / G);
+  *q1 = static_cast<int32_t>(static_cast<int64_t>(nvec) * (rank + 1) / G);
+}
 
 __device__ __forceinline__ Slice make_slice(const float* row, int32_t L, int rank, int G) {
   Slice s;
@@ -234,18 +403,34 @@ __device__ __forceinline__ Slice make_slice(const float* row, int32_t L, int ran
   const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) >> 2) & 3u;
   int32_t head = static_cast<int32_t>((4u - mis) & 3u);
   if (head > L) head = L;
-  const int64_t nvec = static_cast<int64_t>(L - head) >> 2;
-  s.vec0 = head;
-  s.vec = reinterpret_cast<const uint4*>(row + head);
-  s.q0 = nvec * rank / G;
-  s.q1 = nvec * (rank + 1) / G;
-  const int32_t tail0 = head + static_cast<int32_t>(nvec * 4);
+  s.nvec = (L - head) >> 2;
+  int32_t q0, q1;
+  quad_range(s.nvec, rank, G, &q0, &q1);
+  s.vec = reinterpret_cast<const uint4*>(row + head) + q0;
+  s.nq = q1 - q0;
+  s.j0 = head + 4 * q0;
+  const int32_t tail0 = head + 4 * s.nvec;
   s.n_head = rank == 0 ? head : 0;
   s.tail0 = tail0;
   s.n_tail = rank == G - 1 ? L - tail0 : 0;
-  s.lo = rank == 0 ? 0 : head + static_cast<int32_t>(s.q0 * 4);
-  s.hi = rank == G - 1 ? L : head + static_cast<int32_t>(s.q1 * 4);
+  s.lo = rank == 0 ? 0 : s.j0;
+  s.hi = rank == G - 1 ? L : head + 4 * q1;
   return s;
+}
+
+// The unaligned head/tail position of this thread, if any (at most one).
+__device__ __forceinline__ bool edge_position(const Slice& s, int32_t* j) {
+  const int tid = threadIdx.x;
+  if (tid < s.n_head) {
+    *j = tid;
+    return true;
+  }
+  if (tid >= 4 && tid - 4 < s.n_tail) {
+    *j = s.tail0 + (tid - 4);
+    return true;
+  }
+  *j = 0;
+  return false;
 }
 
 // Calls f(valid, key, position) for every position of the slice. Control flow is
@@ -254,30 +439,23 @@ template <class F>
 __device__ __forceinline__ void visit_keys(const Slice& s, F&& f) {
   const int tid = threadIdx.x;
   {
-    bool ok = false;
-    int32_t j = 0;
-    if (tid < s.n_head) {
-      ok = true;
-      j = tid;
-    } else if (tid >= 4 && tid - 4 < s.n_tail) {
-      ok = true;
-      j = s.tail0 + (tid - 4);
-    }
+    int32_t j;
+    const bool ok = edge_position(s, &j);
     const uint32_t key = ok ? order_key(__float_as_uint(s.row[j])) : 0u;
     f(ok, key, j);
   }
-  for (int64_t base = s.q0; base < s.q1; base += static_cast<int64_t>(kUnroll) * kThreads) {
+  for (int32_t base = 0; base < s.nq; base += kUnroll * kThreads) {
     uint4 x[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t q = base + static_cast<int64_t>(u) * kThreads + tid;
-      x[u] = q < s.q1 ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+      const int32_t q = base + u * kThreads + tid;
+      x[u] = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t q = base + static_cast<int64_t>(u) * kThreads + tid;
-      const bool ok = q < s.q1;
-      const int32_t j = s.vec0 + 4 * static_cast<int32_t>(q);
+      const int32_t q = base + u * kThreads + tid;
+      const bool ok = q < s.nq;
+      const int32_t j = s.j0 + 4 * q;
       f(ok, order_key(x[u].x), j);
       f(ok, order_key(x[u].y), j + 1);
       f(ok, order_key(x[u].z), j + 2);
@@ -289,7 +467,8 @@ __device__ __forceinline__ void visit_keys(const Slice& s, F&& f) {
 // ------------------------------------------------------------------ output map
 
 struct OutMap {
-  const int32_t* pt_row;  // paged: this row's page table
+  const int32_t* pt_row;  // paged: this row's page table (global memory)
+  const int32_t* pt_smem; // paged: the same entries staged in shared memory, or null
   int32_t ps;             // page size
   int32_t ps_shift;       // log2(ps) or -1
   int32_t rstart;         // ragged: row start in the packed buffer
@@ -306,7 +485,8 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
       page = j / m.ps;
       off = j - page * m.ps;
     }
-    return __ldg(m.pt_row + page) * m.ps + off;
+    const int32_t phys = m.pt_smem != nullptr ? m.pt_smem[page] : __ldg(m.pt_row + page);
+    return phys * m.ps + off;
   } else if constexpr (F == kRagged) {
     return m.rstart + j;
   } else {
@@ -314,54 +494,411 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
   }
 }
 
-// ------------------------------------------------------------------ passes
+// Every write of a row's output goes through here: slots at or beyond k are
+// dropped. By construction no slot is ever >= k; the check keeps a miscount (say,
+// scores modified while the kernel runs) from writing outside the row.
+template <int F>
+__device__ __forceinline__ void emit(int32_t* out, int32_t k, uint32_t slot, const OutMap& m,
+                                     int32_t j) {
+  if (slot < static_cast<uint32_t>(k)) out[slot] = map_pos<F>(m, j);
+}
 
-// Step 4: winners (key >> shift > prefix) to out[win_base + ...], ties
-// (key >> shift == prefix) to the tie buffer at tie_base + ... (CTA 0's buffer,
-// through distributed shared memory when G > 1).
+// Where candidates go: CTA 0's buffer and counter, and CTA 0's histogram of their
+// top 12 key bits; local (kRemote false) or through distributed shared memory.
+template <bool kRemote>
+struct Sink {
+  uint2* buf;             // local buffer (CTA 0, or G == 1)
+  uint32_t* cnt;          // local counter
+  uint32_t* hist;         // local candidate histogram
+  uint32_t buf_remote;    // cluster addresses of CTA 0's buffer, counter, histogram
+  uint32_t cnt_remote;
+  uint32_t hist_remote;
+  uint32_t cap;
+  uint32_t lambda;        // candidate histogram: bin = min((key - lambda) >> shift, 4095)
+  uint32_t shift;
+
+  __device__ __forceinline__ void put(uint32_t slot, uint32_t key, int32_t j) const {
+    if (slot >= cap) return;
+    if constexpr (kRemote)
+      dsmem_st2(buf_remote + 8u * slot, key, static_cast<uint32_t>(j));
+    else
+      buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
+  }
+  // The last bin (every key at or beyond lambda + 4095 * 2^shift) is not counted
+  // here: it would put most candidates on one shared counter. Its count is n minus
+  // the other bins (select_candidates).
+  __device__ __forceinline__ void count(uint32_t key) const {
+    const uint32_t d = (key - lambda) >> shift;
+    if (d >= static_cast<uint32_t>(kMaxBins - 1)) return;
+    const uint32_t b = static_cast<uint32_t>(hist_index(static_cast<int>(d)));
+    if constexpr (kRemote)
+      dsmem_add(hist_remote + 4u * b, 1u);
+    else
+      atomicAdd(hist + b, 1u);
+  }
+  __device__ __forceinline__ uint32_t reserve(uint32_t n) const {
+    return warp_reserve(cnt, cnt_remote, kRemote, n);
+  }
+};
+
+// ------------------------------------------------------------------ fast tier
+
+// F1a: issue the sample loads of this CTA (the first memory traffic of the row).
+struct Sample {
+  uint32_t key[4 * kSampleQuads];
+  bool ok[kSampleQuads];
+};
+
+__device__ __forceinline__ int32_t sample_stride(int32_t nq) {
+  const int32_t per = kThreads * kSampleQuads;
+  return max(8, (nq + per - 1) / per);
+}
+
+__device__ __forceinline__ void load_sample(const Slice& s, Sample& sm) {
+  const int32_t stride = sample_stride(s.nq);
+#pragma unroll
+  for (int r = 0; r < kSampleQuads; ++r) {
+    const int32_t q = (static_cast<int32_t>(threadIdx.x) + r * kThreads) * stride;
+    sm.ok[r] = q < s.nq;
+    const uint4 x = sm.ok[r] ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+    sm.key[4 * r + 0] = order_key(x.x);
+    sm.key[4 * r + 1] = order_key(x.y);
+    sm.key[4 * r + 2] = order_key(x.z);
+    sm.key[4 * r + 3] = order_key(x.w);
+  }
+}
+
+// Sums this CTA's histogram into CTA 0's `mhist` (G > 1; cluster barrier after).
+__device__ __forceinline__ void merge_into_cta0(const uint32_t* hist, uint32_t* mhist) {
+  const uint32_t m0 = map_rank(smem_addr(mhist), 0);
+  for (int i = threadIdx.x; i < kHistWords; i += kThreads) {
+    const uint32_t v = hist[i];
+    if (v != 0) dsmem_add(m0 + 4u * static_cast<uint32_t>(i), v);
+  }
+  cluster_sync();
+}
+
+// F1b: lambda and the candidate-histogram bin width from the cluster's sample (see
+// the header comment). `hist` and CTA 0's `mhist` are zero on entry; on return
+// `hist` holds garbage and `mhist` is zero. Returns lambda; *shift2 gets the
+// candidate-histogram bin width exponent.
+__device__ __forceinline__ uint32_t sample_lambda(const Slice& s, const Sample& sm, int32_t L,
+                                                  uint32_t k, int G, int rank, uint32_t* hist,
+                                                  uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
+  const int tid = threadIdx.x;
+  // sample size of the whole cluster (every CTA computes the same number)
+  uint32_t ns = 0;
+  for (int r = 0; r < G; ++r) {
+    int32_t q0, q1;
+    quad_range(s.nvec, r, G, &q0, &q1);
+    const int32_t nq = q1 - q0, st = sample_stride(nq);
+    ns += 4u * static_cast<uint32_t>((nq + st - 1) / st);
+  }
+  *shift2 = 0;
+  if (ns == 0) return 0u;
+  // sample ranks a few standard deviations either side of the expected sample rank
+  // of the row's k-th key
+  const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
+  const float dev = 3.0f * sqrtf(mean);
+  uint32_t rs = static_cast<uint32_t>(ceilf(mean + dev)) + 2u;
+  if (rs > ns) rs = ns;
+  const float lo = floorf(mean - dev);
+  const uint32_t rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
+
+  // round 1: coarse bins (top 12 key bits) of both ranks
+#pragma unroll
+  for (int i = 0; i < 4 * kSampleQuads; ++i)
+    if (sm.ok[i / 4]) atomicAdd(&hist[hist_index(static_cast<int>(sm.key[i] >> 20))], 1u);
+  __syncthreads();
+  if (G > 1) merge_into_cta0(hist, mhist);
+  if (rank == 0) {
+    find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs, rs_lo, ctl);
+    if (tid == 0) {
+      // fine window: coarse bins sel_t .. sel2_t, at most 4096 fine bins
+      const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1 - ctl.sel_t) << 20;
+      const int f = max(0, (64 - __clzll(static_cast<long long>(span - 1))) - 12);
+      ctl.win_lo = ctl.sel_t << 20;
+      ctl.win_shift = static_cast<uint32_t>(f);
+      ctl.win_above = ctl.sel2_above;  // sample keys above the window
+    }
+    if (G > 1) {
+      __syncthreads();
+      if (tid > 0 && tid < G) {
+        dsmem_st(map_rank(smem_addr(&ctl.win_lo), tid), ctl.win_lo);
+        dsmem_st(map_rank(smem_addr(&ctl.win_shift), tid), ctl.win_shift);
+        dsmem_st(map_rank(smem_addr(&ctl.win_above), tid), ctl.win_above);
+        dsmem_st(map_rank(smem_addr(&ctl.sel2_t), tid), ctl.sel2_t);
+      }
+      for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+    }
+  }
+  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (G > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+
+  // round 2: fine bins over [win_lo, end of coarse bin sel2_t]
+  const uint32_t win_lo = ctl.win_lo, f = ctl.win_shift, win_above = ctl.win_above;
+  const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1) * (1ull << 20) - win_lo;
+#pragma unroll
+  for (int i = 0; i < 4 * kSampleQuads; ++i) {
+    const uint64_t d = static_cast<uint64_t>(sm.key[i]) - win_lo;  // wraps for keys below
+    if (sm.ok[i / 4] && sm.key[i] >= win_lo && d < span)
+      atomicAdd(&hist[hist_index(static_cast<int>(d >> f))], 1u);
+  }
+  __syncthreads();
+  if (G > 1) merge_into_cta0(hist, mhist);
+  if (rank == 0) {
+    find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs - win_above, rs_lo - win_above, ctl);
+    if (tid == 0) {
+      const uint32_t lam = win_lo + (ctl.sel_t << f);
+      const uint64_t hi = static_cast<uint64_t>(win_lo) + (static_cast<uint64_t>(ctl.sel2_t + 1) << f) - 1;
+      const uint64_t gap = hi > lam ? hi - lam : 0;
+      const int bits = 64 - __clzll(static_cast<long long>(gap));
+      ctl.lambda = lam;
+      ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - 11));
+    }
+    if (G > 1) {
+      __syncthreads();
+      if (tid > 0 && tid < G) {
+        dsmem_st(map_rank(smem_addr(&ctl.lambda), tid), ctl.lambda);
+        dsmem_st(map_rank(smem_addr(&ctl.lambda_shift), tid), ctl.lambda_shift);
+      }
+      for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+    }
+  }
+  if (G > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  *shift2 = ctl.lambda_shift;
+  return ctl.lambda;
+}
+
+// F2: every position with key >= lambda goes to the sink. kPos: lambda is the key
+// of a non-negative value, so "key >= lambda" is "(int)bits >= lambda ^ 2^31";
+// otherwise it is "bits <= ~lambda" (unsigned).
+template <bool kPos>
+__device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
+  if constexpr (kPos)
+    return static_cast<int32_t>(bits) >= static_cast<int32_t>(thr);
+  else
+    return bits <= thr;
+}
+
+template <bool kPos, bool kRemote>
+__device__ __forceinline__ void filter_pass(const Slice& s, uint32_t lambda,
+                                            const Sink<kRemote>& sink) {
+  const int tid = threadIdx.x;
+  const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
+  {
+    int32_t j;
+    const bool ok = edge_position(s, &j);
+    const uint32_t bits = ok ? __float_as_uint(s.row[j]) : 0u;
+    const bool c = ok && is_candidate<kPos>(bits, thr);
+    const uint32_t slot = sink.reserve(c ? 1u : 0u);
+    if (c) {
+      const uint32_t key = order_key(bits);
+      sink.put(slot, key, j);
+      sink.count(key);
+    }
+  }
+  constexpr int U = kFilterUnroll;
+  for (int32_t base = 0; base < s.nq; base += U * kThreads) {
+    uint32_t xs[4 * U];  // the lane's 4U values; indexed by candidate bit below
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t q = base + u * kThreads + tid;
+      const uint4 x = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+      xs[4 * u + 0] = x.x;
+      xs[4 * u + 1] = x.y;
+      xs[4 * u + 2] = x.z;
+      xs[4 * u + 3] = x.w;
+    }
+    uint32_t m = 0;  // bit 4u+c: element c of quad u is a candidate
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool ok = base + u * kThreads + tid < s.nq;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        m |= static_cast<uint32_t>(ok && is_candidate<kPos>(xs[4 * u + c], thr)) << (4 * u + c);
+    }
+    if (__any_sync(kFull, m != 0u)) {
+      uint32_t slot = sink.reserve(__popc(m));
+      while (m != 0u) {  // this lane's candidates only
+        const int i = __ffs(m) - 1;
+        m &= m - 1u;
+        const uint32_t key = order_key(xs[i]);
+        const int32_t j = s.j0 + 4 * (base + (i >> 2) * kThreads + tid) + (i & 3);
+        sink.put(slot++, key, j);
+        sink.count(key);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ selection in a buffer
+
+__device__ __forceinline__ uint64_t hi_bits(uint64_t v, int p) { return p >= 64 ? 0ull : v >> p; }
+
+// F3 / E3 (CTA 0 only): among the c buffered (key, position) entries, all with
+// composite (key:~position) >> p == P, select the `need` largest composites and
+// write them mapped to out[k_above + ...]. h is a scratch histogram.
+template <int F>
+__device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, uint32_t need,
+                                                 uint64_t P, int p, int32_t L, int32_t* out,
+                                                 int32_t k, uint32_t k_above, const OutMap& m,
+                                                 uint32_t* h, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  auto compose = [](uint2 e) -> uint64_t {
+    return (static_cast<uint64_t>(e.x) << 32) | static_cast<uint64_t>(~e.y);
+  };
+  const uint32_t want = need;  // entries to write
+  if (need < c) {
+    const int nb = 32 - __clz(L - 1);  // positions fit in nb bits (L >= 2 here)
+    for (;;) {
+      if (p == 32) {  // key resolved: the ~position bits above nb are all ones
+        const int skip = 32 - nb;
+        P = (P << skip) | ((1ull << skip) - 1ull);
+        p = nb;
+      }
+      // Composites are unique (positions are), so the loop ends with the threshold
+      // bin holding exactly what is still needed, at the latest when p reaches 0;
+      // the test below only bounds the loop should that ever not hold.
+      if (p <= 0) break;
+      const int lo = p > 32 ? 32 : 0;
+      const int w = min(kBufRoundBits, p - lo);
+      const int np = p - w;
+      const uint32_t mask = (1u << w) - 1u;
+      for (int i = tid; i < hist_index(static_cast<int>(mask) + 1); i += kThreads) h[i] = 0;
+      __syncthreads();
+      for (uint32_t i = tid; i < c; i += kThreads) {
+        const uint64_t v = compose(buf[i]);
+        if (hi_bits(v, p) == P)
+          atomicAdd(&h[hist_index(static_cast<int>(static_cast<uint32_t>(v >> np) & mask))], 1u);
+      }
+      __syncthreads();
+      find_threshold(h, 1 << w, need, ctl);
+      const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
+      need -= above;
+      P = (P << w) | t;
+      p = np;
+      if (ct == need) break;
+    }
+  }
+  // every entry whose composite prefix is >= P is selected
+  const uint32_t cpad = (c + kThreads - 1) / kThreads * kThreads;
+  for (uint32_t i = tid; i < cpad; i += kThreads) {
+    bool sel = false;
+    uint2 e = make_uint2(0, 0);
+    if (i < c) {
+      e = buf[i];
+      sel = hi_bits(compose(e), p) >= P;
+    }
+    const uint32_t slot = warp_reserve_bit(&ctl.out_cnt, sel);
+    if (sel && slot < want) emit<F>(out, k, k_above + slot, m, static_cast<int32_t>(e.y));
+  }
+}
+
+// F3 (CTA 0 only): the filter left n candidates in buf and their histogram (bin =
+// min((key - lambda) >> shift, 4095)) in chist. Writes the k largest composites
+// (key, ~position) mapped to out. h may be chist itself: it is used only after
+// chist has been read.
+template <int F>
+__device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, uint32_t k,
+                                                  uint32_t* chist, uint32_t lambda,
+                                                  uint32_t shift, uint2* list, uint32_t* h,
+                                                  int32_t L, int32_t* out, const OutMap& m,
+                                                  Ctl& ctl) {
+  const int tid = threadIdx.x;
+  {  // the last bin holds every candidate the other bins do not
+    uint32_t part = 0;
+    for (int i = tid; i < kMaxBins - 1; i += kThreads) part += chist[hist_index(i)];
+    const uint32_t counted = block_sum(part, ctl);
+    if (tid == 0) chist[hist_index(kMaxBins - 1)] = n - counted;
+    __syncthreads();
+  }
+  find_threshold(chist, kMaxBins, k, ctl);
+  const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
+  if (ct > static_cast<uint32_t>(kListCap)) {
+    select_in_buffer<F>(buf, n, k, 0ull, 64, L, out, static_cast<int32_t>(k), 0u, m, h, ctl);
+    return;
+  }
+  // candidates above the threshold bin are winners; the bin's go to the list
+  const uint32_t npad = (n + kThreads - 1) / kThreads * kThreads;
+  for (uint32_t i = tid; i < npad; i += kThreads) {
+    uint2 e = make_uint2(0, 0);
+    if (i < n) e = buf[i];
+    const uint32_t b = min((e.x - lambda) >> shift, static_cast<uint32_t>(kMaxBins - 1));
+    const bool win = i < n && b > t;
+    const bool tie = i < n && b == t;
+    const uint32_t ws = warp_reserve_bit(&ctl.win_cnt, win);
+    const uint32_t ts = warp_reserve_bit(&ctl.tie_cnt, tie);
+    if (win && ws < above) emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y));
+    if (tie && ts < ct) list[ts] = e;
+  }
+  __syncthreads();
+  const uint32_t need = k - above;  // 1 <= need <= ct
+  if (ct <= static_cast<uint32_t>(kRankDirect)) {
+    // order the bin by counting: entry i takes slot above + (#entries ranked before it)
+    if (static_cast<uint32_t>(tid) < ct) {
+      const uint2 e = list[tid];
+      const uint64_t v = (static_cast<uint64_t>(e.x) << 32) | static_cast<uint64_t>(~e.y);
+      uint32_t r = 0;
+      for (uint32_t j = 0; j < ct; ++j) {
+        const uint2 o = list[j];
+        const uint64_t w = (static_cast<uint64_t>(o.x) << 32) | static_cast<uint64_t>(~o.y);
+        r += w > v ? 1u : 0u;
+      }
+      if (r < need) emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y));
+    }
+    return;
+  }
+  select_in_buffer<F>(list, ct, need, 0ull, 64, L, out, static_cast<int32_t>(k), above, m, h, ctl);
+}
+
+// ------------------------------------------------------------------ exact tier
+
+// E2: winners (key >> shift > prefix) to out[win_base + ...], ties
+// (key >> shift == prefix) to CTA 0's tie buffer at tie_base + ...
 template <int F>
 __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, int shift,
-                                             int32_t* out, uint32_t win_base, uint32_t tie_base,
+                                             int32_t* out, int32_t k, uint32_t win_base,
+                                             uint32_t tie_base,
                                              uint2* ties, uint32_t ties_remote, bool remote,
-                                             const OutMap& m, Ctl& ctl) {
+                                             uint32_t cap, const OutMap& m, Ctl& ctl) {
   const int tid = threadIdx.x;
   auto put_tie = [&](uint32_t slot, uint32_t key, int32_t j) {
+    if (slot >= cap) return;
     if (remote)
       dsmem_st2(ties_remote + 8u * slot, key, static_cast<uint32_t>(j));
     else
       ties[slot] = make_uint2(key, static_cast<uint32_t>(j));
   };
-  {  // unaligned head and tail, at most one position per thread
-    bool ok = false;
-    int32_t j = 0;
-    if (tid < s.n_head) {
-      ok = true;
-      j = tid;
-    } else if (tid >= 4 && tid - 4 < s.n_tail) {
-      ok = true;
-      j = s.tail0 + (tid - 4);
-    }
+  {
+    int32_t j;
+    const bool ok = edge_position(s, &j);
     const uint32_t key = ok ? order_key(__float_as_uint(s.row[j])) : 0u;
     const bool win = ok && (key >> shift) > prefix;
     const bool tie = ok && (key >> shift) == prefix;
-    const uint32_t ws = warp_reserve(&ctl.win_cnt, win ? 1u : 0u);
-    const uint32_t ts = warp_reserve(&ctl.tie_cnt, tie ? 1u : 0u);
-    if (win) out[win_base + ws] = map_pos<F>(m, j);
+    const uint32_t ws = warp_reserve_bit(&ctl.win_cnt, win);
+    const uint32_t ts = warp_reserve_bit(&ctl.tie_cnt, tie);
+    if (win) emit<F>(out, k, win_base + ws, m, j);
     if (tie) put_tie(tie_base + ts, key, j);
   }
-  for (int64_t base = s.q0; base < s.q1; base += static_cast<int64_t>(kUnroll) * kThreads) {
+  for (int32_t base = 0; base < s.nq; base += kUnroll * kThreads) {
     uint4 x[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t q = base + static_cast<int64_t>(u) * kThreads + tid;
-      x[u] = q < s.q1 ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+      const int32_t q = base + u * kThreads + tid;
+      x[u] = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
     }
     uint32_t key[4 * kUnroll];
     uint32_t wb = 0, tb = 0;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t q = base + static_cast<int64_t>(u) * kThreads + tid;
-      const bool ok = q < s.q1;
+      const bool ok = base + u * kThreads + tid < s.nq;
       key[4 * u + 0] = order_key(x[u].x);
       key[4 * u + 1] = order_key(x[u].y);
       key[4 * u + 2] = order_key(x[u].z);
@@ -374,16 +911,15 @@ __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, in
       }
     }
     if (__any_sync(kFull, (wb | tb) != 0u)) {
-      uint32_t ws = warp_reserve(&ctl.win_cnt, __popc(wb));
-      uint32_t ts = warp_reserve(&ctl.tie_cnt, __popc(tb));
+      uint32_t ws = warp_reserve(&ctl.win_cnt, 0u, false, __popc(wb));
+      uint32_t ts = warp_reserve(&ctl.tie_cnt, 0u, false, __popc(tb));
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int64_t q = base + static_cast<int64_t>(u) * kThreads + tid;
-        const int32_t j = s.vec0 + 4 * static_cast<int32_t>(q);
+        const int32_t j = s.j0 + 4 * (base + u * kThreads + tid);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int bit = 4 * u + c;
-          if ((wb >> bit) & 1u) out[win_base + ws++] = map_pos<F>(m, j + c);
+          if ((wb >> bit) & 1u) emit<F>(out, k, win_base + ws++, m, j + c);
           if ((tb >> bit) & 1u) put_tie(tie_base + ts++, key[bit], j + c);
         }
       }
@@ -391,66 +927,11 @@ __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, in
   }
 }
 
-// Step 5 (CTA 0 only): among the c ties (all with key >> shift == prefix) select
-// the `need` largest composites (key, ~position) and write them to
-// out[k_above + ...].
-template <int F>
-__device__ __forceinline__ void refine_ties(const uint2* ties, uint32_t c, uint32_t need,
-                                            int shift, uint32_t prefix, int32_t L, int32_t* out,
-                                            uint32_t k_above, const OutMap& m, uint32_t* h,
-                                            Ctl& ctl) {
-  const int tid = threadIdx.x;
-  auto compose = [](uint2 e) -> uint64_t {
-    return (static_cast<uint64_t>(e.x) << 32) | static_cast<uint64_t>(~e.y);
-  };
-  uint64_t P = prefix;   // known high bits of the composite: composite >> p == P
-  int p = 32 + shift;
-  if (need < c) {
-    const int nb = 32 - __clz(L - 1);  // positions fit in nb bits (L >= 2 here)
-    for (;;) {
-      if (p == 32) {  // key resolved: the ~position bits above nb are all ones
-        const int skip = 32 - nb;
-        P = (P << skip) | ((1ull << skip) - 1ull);
-        p = nb;
-      }
-      const int lo = p > 32 ? 32 : 0;
-      const int w = min(kBufRoundBits, p - lo);
-      const int np = p - w;
-      const uint32_t mask = (1u << w) - 1u;
-      for (int i = tid; i <= static_cast<int>(mask); i += kThreads) h[i] = 0;
-      __syncthreads();
-      for (uint32_t i = tid; i < c; i += kThreads) {
-        const uint64_t v = compose(ties[i]);
-        if ((v >> p) == P) atomicAdd(&h[static_cast<uint32_t>(v >> np) & mask], 1u);
-      }
-      __syncthreads();
-      find_threshold(h, 1 << w, need, ctl);
-      const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
-      need -= above;
-      P = (P << w) | t;
-      p = np;
-      if (ct == need) break;
-    }
-  }
-  // every tie whose composite prefix is >= P is selected
-  const uint32_t cpad = (c + kThreads - 1) / kThreads * kThreads;
-  for (uint32_t i = tid; i < cpad; i += kThreads) {
-    bool sel = false;
-    uint2 e = make_uint2(0, 0);
-    if (i < c) {
-      e = ties[i];
-      sel = (compose(e) >> p) >= P;
-    }
-    const uint32_t slot = warp_reserve(&ctl.out_cnt, sel ? 1u : 0u);
-    if (sel) out[k_above + slot] = map_pos<F>(m, static_cast<int32_t>(e.y));
-  }
-}
-
-// Step 6: key tau is exact and more elements than the tie buffer holds equal it.
+// E4: key tau is exact and more elements than the tie buffer holds equal it.
 // Each CTA scans its slice in position order, writes its winners (key > tau) and
 // the first `quota` of its elements equal to tau.
 template <int F>
-__device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t* out,
+__device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t* out, int32_t k,
                                            uint32_t win_base, uint32_t eq_slot0,
                                            uint32_t quota, const OutMap& m, Ctl& ctl) {
   const int tid = threadIdx.x;
@@ -466,16 +947,16 @@ __device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t
       wb |= static_cast<uint32_t>(ok && key[u] > tau) << u;
       eb |= static_cast<uint32_t>(ok && key[u] == tau) << u;
     }
-    uint32_t ws = warp_reserve(&ctl.win_cnt, __popc(wb));
+    uint32_t ws = warp_reserve(&ctl.win_cnt, 0u, false, __popc(wb));
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if ((wb >> u) & 1u) out[win_base + ws++] = map_pos<F>(m, j0 + u);
+      if ((wb >> u) & 1u) emit<F>(out, k, win_base + ws++, m, j0 + u);
     uint32_t total;
     uint32_t r = taken + block_excl_scan(__popc(eb), ctl, &total);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if ((eb >> u) & 1u) {
-        if (r < quota) out[eq_slot0 + r] = map_pos<F>(m, j0 + u);
+        if (r < quota) emit<F>(out, k, eq_slot0 + r, m, j0 + u);
         ++r;
       }
     }
@@ -494,8 +975,32 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int rank = static_cast<int>(cluster_ctarank());
   const int row = static_cast<int>(blockIdx.x) / G;
 
+  // shared memory: histogram | list | page table | cluster-sum histogram (G > 1) |
+  // candidate/tie buffer
+  uint32_t* hist = dyn;
+  uint2* list = reinterpret_cast<uint2*>(dyn + kHistWords);
+  int32_t* pt_smem = reinterpret_cast<int32_t*>(dyn + 2 * kHistWords);
+  uint32_t* mhist = dyn + 2 * kHistWords + kPtCap;
+  uint2* buf = reinterpret_cast<uint2*>(dyn + (G > 1 ? 3 : 2) * kHistWords + kPtCap);
+  const uint32_t cap = static_cast<uint32_t>(p.tie_cap);
+
+  // independent of the row: clear the histograms and counters while the row's
+  // length is being read
+  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (G > 1 && rank == 0)
+    for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+  if (tid == 0) {
+    ctl.win_cnt = 0;
+    ctl.tie_cnt = 0;
+    ctl.out_cnt = 0;
+    ctl.cand_cnt = 0;
+    ctl.lambda = 0;
+    ctl.lambda_shift = 0;
+  }
+
   OutMap m;
   m.pt_row = nullptr;
+  m.pt_smem = nullptr;
   m.ps = p.page_size;
   m.ps_shift = p.page_shift;
   m.rstart = 0;
@@ -521,24 +1026,128 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     return;
   }
 
-  uint32_t* hist = dyn;                                   // this CTA's histogram
-  uint32_t* mhist = dyn + kMaxBins;                       // cluster sum (CTA 0, G > 1)
-  uint2* ties = reinterpret_cast<uint2*>(dyn + (G > 1 ? 2 : 1) * kMaxBins);
-
-  if (tid == 0) {
-    ctl.win_cnt = 0;
-    ctl.tie_cnt = 0;
-    ctl.out_cnt = 0;
-  }
-  if (G > 1) {
-    if (rank == 0)
-      for (int i = tid; i < kMaxBins; i += kThreads) mhist[i] = 0;
-    cluster_sync();  // all CTAs running, CTA 0's sum histogram cleared
-  }
   const Slice s = make_slice(rowp, L, rank, G);
+  const bool sampled = p.use_filter && static_cast<uint32_t>(L) > cap;
+  Sample sm;
+  if (sampled) load_sample(s, sm);  // first: nothing else queues ahead of it
+  // paged: the row's page table is read now (into registers) and staged in shared
+  // memory after the sample, when the loads have long completed
+  constexpr int kPtPer = kPtCap / kThreads;
+  int32_t pt_reg[F == kPaged ? kPtPer : 1];
+  int32_t pages = 0;
+  if constexpr (F == kPaged) {
+    const int64_t np = (static_cast<int64_t>(L) + p.page_size - 1) / p.page_size;
+    if (np <= kPtCap) {
+      pages = static_cast<int32_t>(np);
+#pragma unroll
+      for (int r = 0; r < kPtPer; ++r) {
+        const int32_t i = tid + r * kThreads;
+        pt_reg[r] = i < pages ? __ldg(m.pt_row + i) : 0;
+      }
+    }
+  }
+  {  // pull the whole slice towards L2 now; every pass below then reads L2
+    const uint64_t bytes = 16ull * static_cast<uint64_t>(s.nq);
+    const uint64_t pieces = (bytes + kPrefetchBytes - 1) / kPrefetchBytes;
+    for (uint64_t i = tid; i < pieces; i += kThreads)
+      prefetch_l2(reinterpret_cast<const char*>(s.vec) + i * kPrefetchBytes,
+                  static_cast<uint32_t>(min(static_cast<uint64_t>(kPrefetchBytes),
+                                            bytes - i * kPrefetchBytes)));
+  }
+  if (G > 1)
+    cluster_sync();  // all CTAs running; CTA 0's histograms and counters cleared
+  else
+    __syncthreads();
 
-  // Steps 2-3: radix rounds over the row until the threshold bin fits the tie
-  // buffer (or the key is exhausted).
+  // ---------------- fast tier
+  if (p.use_filter) {
+    uint32_t shift2 = 0;
+    const uint32_t lambda =
+        sampled ? sample_lambda(s, sm, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl,
+                                &shift2)
+                : 0u;
+    if constexpr (F == kPaged) {
+      if (pages > 0) {
+#pragma unroll
+        for (int r = 0; r < kPtPer; ++r) {
+          const int32_t i = tid + r * kThreads;
+          if (i < pages) pt_smem[i] = pt_reg[r];
+        }
+        m.pt_smem = pt_smem;  // visible to all threads after the next barrier
+      }
+    }
+    // the candidate histogram: CTA 0's mhist when G > 1, else hist (cleared here)
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+    if (G > 1) {
+      cluster_sync();  // CTA 0's mhist is zero again
+      Sink<true> rs;
+      rs.buf = buf;
+      rs.cnt = &ctl.cand_cnt;
+      rs.hist = mhist;
+      rs.buf_remote = map_rank(smem_addr(buf), 0);
+      rs.cnt_remote = map_rank(smem_addr(&ctl.cand_cnt), 0);
+      rs.hist_remote = map_rank(smem_addr(mhist), 0);
+      rs.cap = cap;
+      rs.lambda = lambda;
+      rs.shift = shift2;
+      if (lambda >= 0x80000000u)
+        filter_pass<true>(s, lambda, rs);
+      else
+        filter_pass<false>(s, lambda, rs);
+    } else {
+      __syncthreads();
+      Sink<false> ls;
+      ls.buf = buf;
+      ls.cnt = &ctl.cand_cnt;
+      ls.hist = hist;
+      ls.buf_remote = ls.cnt_remote = ls.hist_remote = 0u;
+      ls.cap = cap;
+      ls.lambda = lambda;
+      ls.shift = shift2;
+      if (lambda >= 0x80000000u)
+        filter_pass<true>(s, lambda, ls);
+      else
+        filter_pass<false>(s, lambda, ls);
+    }
+    uint32_t n_cand;
+    if (G > 1) {
+      cluster_sync();  // every candidate is in CTA 0's buffer
+      if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
+      cluster_sync();
+      n_cand = ctl.n_cand;
+    } else {
+      __syncthreads();
+      n_cand = ctl.cand_cnt;
+    }
+    if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap) {
+      if (rank == 0)
+        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), G > 1 ? mhist : hist, lambda,
+                             shift2, list, hist, L, out, m, ctl);
+      return;
+    }
+    // too few (lambda above the k-th key) or too many candidates: exact tier
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+    if (G > 1) {
+      if (rank == 0)
+        for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+      cluster_sync();
+    } else {
+      __syncthreads();
+    }
+  }
+
+  // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
+  if constexpr (F == kPaged) {
+    if (pages > 0 && m.pt_smem == nullptr) {
+#pragma unroll
+      for (int r = 0; r < kPtPer; ++r) {
+        const int32_t i = tid + r * kThreads;
+        if (i < pages) pt_smem[i] = pt_reg[r];
+      }
+      __syncthreads();
+      m.pt_smem = pt_smem;
+    }
+  }
   uint32_t need = static_cast<uint32_t>(k);  // winners still to find at or below the bin
   uint32_t prefix = 0;                       // known high bits of the threshold key
   int shift = 32;                            // prefix == threshold key >> shift
@@ -549,52 +1158,31 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     const int w = min(kRowRoundBits, shift);
     const int nshift = shift - w;
     const uint32_t mask = (1u << w) - 1u;
-    for (int i = tid; i <= static_cast<int>(mask); i += kThreads) hist[i] = 0;
-    __syncthreads();
+    if (shift != 32) {
+      for (int i = tid; i < hist_index(static_cast<int>(mask) + 1); i += kThreads) hist[i] = 0;
+      __syncthreads();
+    }
     visit_keys(s, [&](bool ok, uint32_t key, int32_t) {
       if (ok && __funnelshift_rc(key, 0u, shift) == prefix)
-        atomicAdd(&hist[(key >> nshift) & mask], 1u);
+        atomicAdd(&hist[hist_index(static_cast<int>((key >> nshift) & mask))], 1u);
     });
     __syncthreads();
-    uint32_t t, above, c;
+    const Sel sel = threshold_of(hist, mhist, 1 << w, need, G, rank, ctl);
     if (G == 1) {
-      find_threshold(hist, 1 << w, need, ctl);
-      t = ctl.sel_t;
-      above = ctl.sel_above;
-      c = ctl.sel_count;
-      above_local += above;
-      tie_local = c;
+      above_local += sel.above;
+      tie_local = sel.count;
     } else {
-      const uint32_t m0 = map_rank(smem_addr(mhist), 0);
-      for (int i = tid; i <= static_cast<int>(mask); i += kThreads) {
-        const uint32_t v = hist[i];
-        if (v != 0) dsmem_add(m0 + 4u * static_cast<uint32_t>(i), v);
-      }
-      cluster_sync();
-      if (rank == 0) {
-        find_threshold(mhist, 1 << w, need, ctl);
-        if (tid > 0 && tid < G) {
-          dsmem_st(map_rank(smem_addr(&ctl.sel_t), tid), ctl.sel_t);
-          dsmem_st(map_rank(smem_addr(&ctl.sel_above), tid), ctl.sel_above);
-          dsmem_st(map_rank(smem_addr(&ctl.sel_count), tid), ctl.sel_count);
-        }
-        for (int i = tid; i <= static_cast<int>(mask); i += kThreads) mhist[i] = 0;
-      }
-      cluster_sync();
-      t = ctl.sel_t;
-      above = ctl.sel_above;
-      c = ctl.sel_count;
       uint32_t part = 0;
       for (int i = tid; i <= static_cast<int>(mask); i += kThreads)
-        part += static_cast<uint32_t>(i) > t ? hist[i] : 0u;
-      tie_local = hist[t];
+        part += static_cast<uint32_t>(i) > sel.t ? hist[hist_index(i)] : 0u;
+      tie_local = hist[hist_index(static_cast<int>(sel.t))];
       above_local += block_sum(part, ctl);
     }
-    need -= above;
-    prefix = (prefix << w) | t;
+    need -= sel.above;
+    prefix = (prefix << w) | sel.t;
     shift = nshift;
-    cnt = c;
-    if (cnt <= static_cast<uint32_t>(p.tie_cap) || shift == 0) break;
+    cnt = sel.count;
+    if (cnt <= cap || shift == 0) break;
   }
 
   const uint32_t k_above = static_cast<uint32_t>(k) - need;  // winners above the bin
@@ -611,20 +1199,22 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     }
   }
 
-  if (cnt <= static_cast<uint32_t>(p.tie_cap)) {
+  if (cnt <= cap) {
     const bool remote = G > 1 && rank != 0;
-    const uint32_t ties_remote = G > 1 ? map_rank(smem_addr(ties), 0) : 0u;
-    scatter_pass<F>(s, prefix, shift, out, win_base, tie_base, ties, ties_remote, remote, m, ctl);
+    const uint32_t ties_remote = G > 1 ? map_rank(smem_addr(buf), 0) : 0u;
+    scatter_pass<F>(s, prefix, shift, out, k, win_base, tie_base, buf, ties_remote, remote, cap, m,
+                    ctl);
     if (G > 1)
       cluster_sync();  // CTA 0 now holds every tie
     else
       __syncthreads();
-    if (rank == 0) refine_ties<F>(ties, cnt, need, shift, prefix, L, out, k_above, m, hist, ctl);
+    if (rank == 0)
+      select_in_buffer<F>(buf, cnt, need, prefix, 32 + shift, L, out, k, k_above, m, hist, ctl);
   } else {
     // tie_base is this CTA's first position among the elements equal to prefix
     const uint32_t quota = tie_base >= need ? 0u : min(need - tie_base, tie_local);
     const uint32_t eq_slot0 = k_above + min(tie_base, need);
-    emit_equal<F>(s, prefix, out, win_base, eq_slot0, quota, m, ctl);
+    emit_equal<F>(s, prefix, out, k, win_base, eq_slot0, quota, m, ctl);
   }
 }
 
@@ -658,7 +1248,8 @@ cudaError_t prepare_form() {
 }  // namespace
 
 size_t smem_bytes(int g, int tie_cap) {
-  return sizeof(uint32_t) * kMaxBins * (g > 1 ? 2 : 1) + sizeof(uint2) * static_cast<size_t>(tie_cap);
+  return sizeof(uint32_t) * (kHistWords * (g > 1 ? 3 : 2) + kPtCap) +
+         sizeof(uint2) * static_cast<size_t>(tie_cap);
 }
 
 cudaError_t prepare_device() {

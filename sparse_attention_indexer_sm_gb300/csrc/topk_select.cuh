@@ -28,6 +28,7 @@ struct Params {
   int32_t k;
   int32_t tie_cap;             // <= kTieCapMax
   int32_t batch;
+  int32_t use_filter;          // 1: try the sampled-threshold filter pass first
 };
 
 // Dynamic shared memory one CTA needs for a cluster of `g` CTAs.

@@ -31,9 +31,10 @@ def pkg():
 
 
 @contextlib.contextmanager
-def settings(pkg, split=None, tie_cap=None):
+def settings(pkg, split=None, tie_cap=None, fast=None):
     prev_split = pkg.topk_set_row_split(split) if split is not None else None
     prev_cap = pkg.topk_set_tie_capacity(tie_cap) if tie_cap is not None else None
+    prev_fast = pkg.topk_set_fast_tier(fast) if fast is not None else None
     try:
         yield
     finally:
@@ -41,6 +42,8 @@ def settings(pkg, split=None, tie_cap=None):
             pkg.topk_set_row_split(prev_split)
         if tie_cap is not None:
             pkg.topk_set_tie_capacity(prev_cap)
+        if fast is not None:
+            pkg.topk_set_fast_tier(prev_fast)
 
 
 def run_gpu(pkg, w, stream=None) -> np.ndarray:
@@ -125,26 +128,60 @@ def _mixed(seed, dist, batch=6, stride=20000, k=1024, dup=True, form="paged"):
     return w
 
 
+@pytest.mark.parametrize("fast", [True, False])
 @pytest.mark.parametrize("split", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("dist", ["normal", "decode", "banded", "narrow", "subnormal", "heavy_tail"])
-def test_every_row_split(pkg, split, dist):
-    """Single-CTA and cluster row-split paths give the oracle's set (cross-path A/B
-    of the PR #36004 page's index-set comparison, restated per split)."""
+def test_every_row_split(pkg, split, dist, fast):
+    """Single-CTA and cluster row-split paths, with and without the sampled filter
+    tier, give the oracle's set (cross-path A/B of the PR #36004 page's index-set
+    comparison, restated per path)."""
     w = _mixed(100 + split, dist)
+    with settings(pkg, split=split, fast=fast):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("fast", [True, False])
+@pytest.mark.parametrize("tie_cap", [0, 1, 16, 300, 4096])
+@pytest.mark.parametrize("split", [1, 4])
+@pytest.mark.parametrize("dist", ["decode", "banded", "narrow", "subnormal"])
+def test_tie_buffer_capacity(pkg, tie_cap, split, dist, fast):
+    """Small buffers force the filter's overflow fallback, more radix rounds and the
+    position-ordered rescan."""
+    w = _mixed(200 + tie_cap, dist, k=2048)
+    with settings(pkg, split=split, tie_cap=tie_cap, fast=fast):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("split", [1, 2, 8])
+def test_misleading_sample_falls_back(pkg, split):
+    """Large values placed exactly on the sampled quads make the sampled threshold
+    too high (fewer than k candidates); the verify step must send the row to the
+    exact tier. Every 16-byte quad position is made large in turn for one row, so
+    whatever the sample stride, some rows are misled."""
+    batch, stride, k = 16, 32768, 1024
+    g = workloads.rng(800 + split)
+    scores = workloads.random_rows(g, batch, stride, "normal")
+    for b in range(batch):
+        period = 2 ** (b % 8 + 1)  # quad strides 2 .. 256
+        quads = np.arange(0, stride // 4, period)
+        for c in range(4):
+            scores[b, quads * 4 + c] = 100.0 + g.standard_normal(quads.shape[0]).astype(np.float32)
+    seq = np.full(batch, stride, np.int32)
+    w = workloads.Workload("misleading_sample", "raw", k, scores, seq)
     with settings(pkg, split=split):
         got = run_gpu(pkg, w)
     assert_parity(w, got)
 
 
-@pytest.mark.parametrize("tie_cap", [0, 1, 16, 300, 4096])
-@pytest.mark.parametrize("split", [1, 4])
-@pytest.mark.parametrize("dist", ["decode", "banded", "narrow", "subnormal"])
-def test_tie_buffer_capacity(pkg, tie_cap, split, dist):
-    """Small tie buffers force more radix rounds and the position-ordered rescan."""
-    w = _mixed(200 + tie_cap, dist, k=2048)
-    with settings(pkg, split=split, tie_cap=tie_cap):
+@pytest.mark.parametrize("form", ["raw", "paged"])
+@pytest.mark.parametrize("batch", [1, 64, 256])
+def test_exact_tier_alone_on_decode_sweep(pkg, batch, form):
+    w = workloads.config3(batch, form)
+    with settings(pkg, fast=False):
         got = run_gpu(pkg, w)
-    assert_parity(w, got)
+    assert_parity(w, got, check_rows=8)
 
 
 @pytest.mark.parametrize("split", [1, 2, 16])
