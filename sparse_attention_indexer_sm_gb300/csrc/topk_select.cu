@@ -62,6 +62,7 @@ namespace {
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;            // 128-bit loads in flight per thread per step (exact tier)
 constexpr int kFilterUnroll = 8;      // 128-bit loads in flight per thread in the filter
+constexpr int kMaskIters = 4;         // filter iterations whose masks are decoded together
 constexpr int kRowRoundBits = 12;     // histogram width of the rounds over the row
 constexpr int kBufRoundBits = 12;     // histogram width of the rounds over a buffer
 constexpr int kSampleQuads = 2;       // sampled 16-byte quads per thread
@@ -84,6 +85,8 @@ struct Ctl {
   uint32_t cand_cnt;                  // candidates found by the filter (CTA 0)
   uint32_t n_cand;                    // cand_cnt of CTA 0, broadcast
   uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
+  uint32_t ns;                        // valid sample size (CTA 0)
+  uint32_t gbase;                     // first buffer slot of the current filter group
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
@@ -391,10 +394,12 @@ struct Slice {
   int32_t lo, hi;         // the CTA's positions as one range [lo, hi)
 };
 
+// Quads [q0, q1) of CTA `rank` of G (a power of two) in an aligned body of nvec.
 __device__ __forceinline__ void quad_range(int32_t nvec, int rank, int G, int32_t* q0,
                                            int32_t* q1) {
-  *q0 = static_cast<int32_t>(static_cast<int64_t>(nvec) * rank / G);
-  *q1 = static_cast<int32_t>(static_cast<int64_t>(nvec) * (rank + 1) / G);
+  const int lg = __ffs(G) - 1;
+  *q0 = static_cast<int32_t>((static_cast<uint64_t>(nvec) * static_cast<uint32_t>(rank)) >> lg);
+  *q1 = static_cast<int32_t>((static_cast<uint64_t>(nvec) * static_cast<uint32_t>(rank + 1)) >> lg);
 }
 
 __device__ __forceinline__ Slice make_slice(const float* row, int32_t L, int rank, int G) {
@@ -464,6 +469,16 @@ __device__ __forceinline__ void visit_keys(const Slice& s, F&& f) {
   }
 }
 
+// Bulk L2 prefetch of a slice's aligned body, in 16 KB pieces over the threads.
+__device__ __forceinline__ void prefetch_slice(const Slice& s) {
+  const uint64_t bytes = 16ull * static_cast<uint64_t>(s.nq);
+  const uint64_t pieces = (bytes + kPrefetchBytes - 1) / kPrefetchBytes;
+  for (uint64_t i = threadIdx.x; i < pieces; i += kThreads)
+    prefetch_l2(reinterpret_cast<const char*>(s.vec) + i * kPrefetchBytes,
+                static_cast<uint32_t>(min(static_cast<uint64_t>(kPrefetchBytes),
+                                          bytes - i * kPrefetchBytes)));
+}
+
 // ------------------------------------------------------------------ output map
 
 struct OutMap {
@@ -503,50 +518,15 @@ __device__ __forceinline__ void emit(int32_t* out, int32_t k, uint32_t slot, con
   if (slot < static_cast<uint32_t>(k)) out[slot] = map_pos<F>(m, j);
 }
 
-// Where candidates go: CTA 0's buffer and counter, and CTA 0's histogram of their
-// top 12 key bits; local (kRemote false) or through distributed shared memory.
-template <bool kRemote>
-struct Sink {
-  uint2* buf;             // local buffer (CTA 0, or G == 1)
-  uint32_t* cnt;          // local counter
-  uint32_t* hist;         // local candidate histogram
-  uint32_t buf_remote;    // cluster addresses of CTA 0's buffer, counter, histogram
-  uint32_t cnt_remote;
-  uint32_t hist_remote;
-  uint32_t cap;
-  uint32_t lambda;        // candidate histogram: bin = min((key - lambda) >> shift, 4095)
-  uint32_t shift;
-
-  __device__ __forceinline__ void put(uint32_t slot, uint32_t key, int32_t j) const {
-    if (slot >= cap) return;
-    if constexpr (kRemote)
-      dsmem_st2(buf_remote + 8u * slot, key, static_cast<uint32_t>(j));
-    else
-      buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
-  }
-  // The last bin (every key at or beyond lambda + 4095 * 2^shift) is not counted
-  // here: it would put most candidates on one shared counter. Its count is n minus
-  // the other bins (select_candidates).
-  __device__ __forceinline__ void count(uint32_t key) const {
-    const uint32_t d = (key - lambda) >> shift;
-    if (d >= static_cast<uint32_t>(kMaxBins - 1)) return;
-    const uint32_t b = static_cast<uint32_t>(hist_index(static_cast<int>(d)));
-    if constexpr (kRemote)
-      dsmem_add(hist_remote + 4u * b, 1u);
-    else
-      atomicAdd(hist + b, 1u);
-  }
-  __device__ __forceinline__ uint32_t reserve(uint32_t n) const {
-    return warp_reserve(cnt, cnt_remote, kRemote, n);
-  }
-};
-
 // ------------------------------------------------------------------ fast tier
 
-// F1a: issue the sample loads of this CTA (the first memory traffic of the row).
+// F1a: the strided sample of a CTA's part of the row: keys of the sampled 16-byte
+// quads and the row position of each quad's first element (INT32_MAX when the
+// thread has no quad). An element counts only if its position is below the row's
+// length, which for the raw and paged forms is read while the sample is in flight.
 struct Sample {
   uint32_t key[4 * kSampleQuads];
-  bool ok[kSampleQuads];
+  int32_t j[kSampleQuads];
 };
 
 __device__ __forceinline__ int32_t sample_stride(int32_t nq) {
@@ -559,13 +539,18 @@ __device__ __forceinline__ void load_sample(const Slice& s, Sample& sm) {
 #pragma unroll
   for (int r = 0; r < kSampleQuads; ++r) {
     const int32_t q = (static_cast<int32_t>(threadIdx.x) + r * kThreads) * stride;
-    sm.ok[r] = q < s.nq;
-    const uint4 x = sm.ok[r] ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+    const bool ok = q < s.nq;
+    const uint4 x = ok ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
     sm.key[4 * r + 0] = order_key(x.x);
     sm.key[4 * r + 1] = order_key(x.y);
     sm.key[4 * r + 2] = order_key(x.z);
     sm.key[4 * r + 3] = order_key(x.w);
+    sm.j[r] = ok ? s.j0 + 4 * q : INT32_MAX;
   }
+}
+
+__device__ __forceinline__ bool sample_valid(const Sample& sm, int i, int32_t L) {
+  return sm.j[i / 4] < L - (i & 3);
 }
 
 // Sums this CTA's histogram into CTA 0's `mhist` (G > 1; cluster barrier after).
@@ -579,47 +564,62 @@ __device__ __forceinline__ void merge_into_cta0(const uint32_t* hist, uint32_t* 
 }
 
 // F1b: lambda and the candidate-histogram bin width from the cluster's sample (see
-// the header comment). `hist` and CTA 0's `mhist` are zero on entry; on return
-// `hist` holds garbage and `mhist` is zero. Returns lambda; *shift2 gets the
-// candidate-histogram bin width exponent.
-__device__ __forceinline__ uint32_t sample_lambda(const Slice& s, const Sample& sm, int32_t L,
+// the header comment). `hist`, CTA 0's `mhist` and CTA 0's ctl.ns are zero on
+// entry; on return `hist` holds garbage and `mhist` is zero. Returns lambda;
+// *shift2 gets the candidate-histogram bin width exponent.
+__device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice& s, int32_t L,
                                                   uint32_t k, int G, int rank, uint32_t* hist,
                                                   uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
   const int tid = threadIdx.x;
-  // sample size of the whole cluster (every CTA computes the same number)
-  uint32_t ns = 0;
-  for (int r = 0; r < G; ++r) {
-    int32_t q0, q1;
-    quad_range(s.nvec, r, G, &q0, &q1);
-    const int32_t nq = q1 - q0, st = sample_stride(nq);
-    ns += 4u * static_cast<uint32_t>((nq + st - 1) / st);
-  }
-  *shift2 = 0;
-  if (ns == 0) return 0u;
-  // sample ranks a few standard deviations either side of the expected sample rank
-  // of the row's k-th key
-  const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
-  const float dev = 3.0f * sqrtf(mean);
-  uint32_t rs = static_cast<uint32_t>(ceilf(mean + dev)) + 2u;
-  if (rs > ns) rs = ns;
-  const float lo = floorf(mean - dev);
-  const uint32_t rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
-
-  // round 1: coarse bins (top 12 key bits) of both ranks
+  // round 1: coarse bins (top 12 key bits); the valid sample size goes to CTA 0
+  uint32_t mine = 0;
 #pragma unroll
-  for (int i = 0; i < 4 * kSampleQuads; ++i)
-    if (sm.ok[i / 4]) atomicAdd(&hist[hist_index(static_cast<int>(sm.key[i] >> 20))], 1u);
+  for (int i = 0; i < 4 * kSampleQuads; ++i) {
+    if (sample_valid(sm, i, L)) {
+      atomicAdd(&hist[hist_index(static_cast<int>(sm.key[i] >> 20))], 1u);
+      ++mine;
+    }
+  }
+  prefetch_slice(s);  // the sample has arrived: now the bulk of the slice
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kFull, mine, off);
+  if ((tid & 31) == 0 && mine != 0) {
+    if (G == 1)
+      atomicAdd(&ctl.ns, mine);
+    else
+      dsmem_add(map_rank(smem_addr(&ctl.ns), 0), mine);
+  }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist, mhist);
+  // sample ranks a few standard deviations either side of the expected sample rank
+  // of the row's k-th key (CTA 0 only)
+  uint32_t rs = 0, rs_lo = 0;
   if (rank == 0) {
-    find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs, rs_lo, ctl);
+    const uint32_t ns = ctl.ns;
+    if (ns != 0) {
+      const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
+      const float dev = 3.0f * sqrtf(mean);
+      rs = static_cast<uint32_t>(ceilf(mean + dev)) + 2u;
+      if (rs > ns) rs = ns;
+      const float lo = floorf(mean - dev);
+      rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
+      if (rs_lo > rs) rs_lo = rs;
+      find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs, rs_lo, ctl);
+    }
     if (tid == 0) {
-      // fine window: coarse bins sel_t .. sel2_t, at most 4096 fine bins
-      const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1 - ctl.sel_t) << 20;
-      const int f = max(0, (64 - __clzll(static_cast<long long>(span - 1))) - 12);
-      ctl.win_lo = ctl.sel_t << 20;
-      ctl.win_shift = static_cast<uint32_t>(f);
-      ctl.win_above = ctl.sel2_above;  // sample keys above the window
+      if (ns != 0) {
+        // fine window: coarse bins sel_t .. sel2_t, at most 4096 fine bins
+        const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1 - ctl.sel_t) << 20;
+        const int f = max(0, (64 - __clzll(static_cast<long long>(span - 1))) - 12);
+        ctl.win_lo = ctl.sel_t << 20;
+        ctl.win_shift = static_cast<uint32_t>(f);
+        ctl.win_above = ctl.sel2_above;  // sample keys above the window
+      } else {  // no sample below the row's length: keep everything
+        ctl.sel2_t = 0;
+        ctl.win_lo = 0;
+        ctl.win_shift = 8;
+        ctl.win_above = 0;
+      }
     }
     if (G > 1) {
       __syncthreads();
@@ -644,20 +644,26 @@ __device__ __forceinline__ uint32_t sample_lambda(const Slice& s, const Sample& 
 #pragma unroll
   for (int i = 0; i < 4 * kSampleQuads; ++i) {
     const uint64_t d = static_cast<uint64_t>(sm.key[i]) - win_lo;  // wraps for keys below
-    if (sm.ok[i / 4] && sm.key[i] >= win_lo && d < span)
+    if (sample_valid(sm, i, L) && sm.key[i] >= win_lo && d < span)
       atomicAdd(&hist[hist_index(static_cast<int>(d >> f))], 1u);
   }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist, mhist);
   if (rank == 0) {
-    find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs - win_above, rs_lo - win_above, ctl);
+    if (rs != 0) find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs - win_above, rs_lo - win_above, ctl);
     if (tid == 0) {
-      const uint32_t lam = win_lo + (ctl.sel_t << f);
-      const uint64_t hi = static_cast<uint64_t>(win_lo) + (static_cast<uint64_t>(ctl.sel2_t + 1) << f) - 1;
-      const uint64_t gap = hi > lam ? hi - lam : 0;
-      const int bits = 64 - __clzll(static_cast<long long>(gap));
-      ctl.lambda = lam;
-      ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - 11));
+      if (rs != 0) {
+        const uint32_t lam = win_lo + (ctl.sel_t << f);
+        const uint64_t hi =
+            static_cast<uint64_t>(win_lo) + (static_cast<uint64_t>(ctl.sel2_t + 1) << f) - 1;
+        const uint64_t gap = hi > lam ? hi - lam : 0;
+        const int bits = 64 - __clzll(static_cast<long long>(gap));
+        ctl.lambda = lam;
+        ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - 11));
+      } else {
+        ctl.lambda = 0;
+        ctl.lambda_shift = 20;
+      }
     }
     if (G > 1) {
       __syncthreads();
@@ -676,9 +682,9 @@ __device__ __forceinline__ uint32_t sample_lambda(const Slice& s, const Sample& 
   return ctl.lambda;
 }
 
-// F2: every position with key >= lambda goes to the sink. kPos: lambda is the key
-// of a non-negative value, so "key >= lambda" is "(int)bits >= lambda ^ 2^31";
-// otherwise it is "bits <= ~lambda" (unsigned).
+// F2: "key >= lambda" on raw fp32 bits. kPos: lambda is the key of a non-negative
+// value, so the test is "(int)bits >= lambda ^ 2^31"; otherwise "bits <= ~lambda"
+// (unsigned).
 template <bool kPos>
 __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
   if constexpr (kPos)
@@ -687,55 +693,112 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
     return bits <= thr;
 }
 
-template <bool kPos, bool kRemote>
-__device__ __forceinline__ void filter_pass(const Slice& s, uint32_t lambda,
-                                            const Sink<kRemote>& sink) {
+// F2: stream the slice, keep per lane a 32-bit candidate mask per iteration (8
+// quads), and every kMaskIters iterations turn the masks into positions written
+// compactly into CTA 0's buffer (entry .y; .x is filled by fill_candidates). The
+// slots come from one block-wide prefix count per group and one reservation on
+// CTA 0's counter per group (a distributed-shared-memory atomic in every CTA when
+// the cluster has several). Slots at or beyond `cap` are counted but not written.
+template <bool kPos>
+__device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint2* buf,
+                                                 uint32_t buf_remote, uint32_t cnt_remote,
+                                                 bool remote, bool cluster_cnt, uint32_t cap,
+                                                 Ctl& ctl) {
   const int tid = threadIdx.x;
   const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
-  {
-    int32_t j;
-    const bool ok = edge_position(s, &j);
-    const uint32_t bits = ok ? __float_as_uint(s.row[j]) : 0u;
-    const bool c = ok && is_candidate<kPos>(bits, thr);
-    const uint32_t slot = sink.reserve(c ? 1u : 0u);
-    if (c) {
-      const uint32_t key = order_key(bits);
-      sink.put(slot, key, j);
-      sink.count(key);
-    }
-  }
   constexpr int U = kFilterUnroll;
-  for (int32_t base = 0; base < s.nq; base += U * kThreads) {
-    uint32_t xs[4 * U];  // the lane's 4U values; indexed by candidate bit below
+  constexpr int MI = kMaskIters;
+  constexpr int32_t kStep = U * kThreads;
+  int32_t ej;
+  const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
+  bool first = true;
+  for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
+    uint32_t mk[MI];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int32_t q = base + u * kThreads + tid;
-      const uint4 x = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
-      xs[4 * u + 0] = x.x;
-      xs[4 * u + 1] = x.y;
-      xs[4 * u + 2] = x.z;
-      xs[4 * u + 3] = x.w;
+    for (int it = 0; it < MI; ++it) {
+      const int32_t base = gbase + it * kStep;
+      uint32_t m = 0;
+      if (base < s.nq) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int32_t q = base + u * kThreads + tid;
+          x[u] = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const bool ok = base + u * kThreads + tid < s.nq;
+          m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].x, thr)) << (4 * u + 0);
+          m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].y, thr)) << (4 * u + 1);
+          m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].z, thr)) << (4 * u + 2);
+          m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].w, thr)) << (4 * u + 3);
+        }
+      }
+      mk[it] = m;
     }
-    uint32_t m = 0;  // bit 4u+c: element c of quad u is a candidate
+    const bool with_edge = first && edge;
+    uint32_t n = with_edge ? 1u : 0u;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool ok = base + u * kThreads + tid < s.nq;
+    for (int it = 0; it < MI; ++it) n += static_cast<uint32_t>(__popc(mk[it]));
+    uint32_t total;
+    const uint32_t off = block_excl_scan(n, ctl, &total);
+    if (total != 0) {
+      if (tid == 0)
+        ctl.gbase = cluster_cnt ? dsmem_fetch_add(cnt_remote, total) : atomicAdd(&ctl.cand_cnt, total);
+      __syncthreads();
+      uint32_t slot = ctl.gbase + off;
+      auto put = [&](int32_t j) {
+        if (slot < cap) {
+          if (remote)
+            dsmem_st(buf_remote + 8u * slot + 4u, static_cast<uint32_t>(j));
+          else
+            buf[slot].y = static_cast<uint32_t>(j);
+        }
+        ++slot;
+      };
+      if (with_edge) put(ej);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        m |= static_cast<uint32_t>(ok && is_candidate<kPos>(xs[4 * u + c], thr)) << (4 * u + c);
+      for (int it = 0; it < MI; ++it) {
+        uint32_t mm = mk[it];
+        const int32_t base = gbase + it * kStep;
+        while (mm != 0u) {
+          const int b = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          put(s.j0 + 4 * (base + (b >> 2) * kThreads + tid) + (b & 3));
+        }
+      }
     }
-    if (__any_sync(kFull, m != 0u)) {
-      uint32_t slot = sink.reserve(__popc(m));
-      while (m != 0u) {  // this lane's candidates only
-        const int i = __ffs(m) - 1;
-        m &= m - 1u;
-        const uint32_t key = order_key(xs[i]);
-        const int32_t j = s.j0 + 4 * (base + (i >> 2) * kThreads + tid) + (i & 3);
-        sink.put(slot++, key, j);
-        sink.count(key);
+    first = false;
+  }
+}
+
+// F2 (CTA 0 only): the n buffered positions get their keys, read back (from L2)
+// in batches of four per thread, and the candidate histogram (bin = (key - lambda)
+// >> shift; the last bin is filled in by select_candidates) is counted in `chist`,
+// which is zero on entry.
+__device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, uint32_t n,
+                                                uint32_t lambda, uint32_t shift,
+                                                uint32_t* chist) {
+  const int tid = threadIdx.x;
+  for (uint32_t i0 = tid; i0 < n; i0 += 4 * kThreads) {
+    uint32_t bits[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t i = i0 + r * kThreads;
+      bits[r] = i < n ? __float_as_uint(__ldg(row + buf[i].y)) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t i = i0 + r * kThreads;
+      if (i < n) {
+        const uint32_t key = order_key(bits[r]);
+        buf[i].x = key;
+        const uint32_t d = (key - lambda) >> shift;
+        if (d < static_cast<uint32_t>(kMaxBins - 1)) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
       }
     }
   }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------ selection in a buffer
@@ -994,6 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     ctl.tie_cnt = 0;
     ctl.out_cnt = 0;
     ctl.cand_cnt = 0;
+    ctl.ns = 0;
     ctl.lambda = 0;
     ctl.lambda_shift = 0;
   }
@@ -1007,6 +1071,19 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int32_t seq = p.seq_lens[row];
   const float* rowp;
   int32_t L;
+  // raw, paged: the row's start does not depend on its length, so the sample is
+  // loaded (over the whole row stride; elements at or past the length are ignored
+  // later) while the length is still on its way
+  Sample sm;
+  bool sample_loaded = false;
+  if constexpr (F != kRagged) {
+    if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
+      load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
+                             static_cast<int32_t>(p.row_stride), rank, G),
+                  sm);
+      sample_loaded = true;
+    }
+  }
   if constexpr (F == kRagged) {
     m.rstart = p.row_starts[row];
     rowp = p.scores + m.rstart;
@@ -1028,8 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   const Slice s = make_slice(rowp, L, rank, G);
   const bool sampled = p.use_filter && static_cast<uint32_t>(L) > cap;
-  Sample sm;
-  if (sampled) load_sample(s, sm);  // first: nothing else queues ahead of it
+  if (sampled && !sample_loaded) load_sample(s, sm);
   // paged: the row's page table is read now (into registers) and staged in shared
   // memory after the sample, when the loads have long completed
   constexpr int kPtPer = kPtCap / kThreads;
@@ -1046,14 +1122,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
     }
   }
-  {  // pull the whole slice towards L2 now; every pass below then reads L2
-    const uint64_t bytes = 16ull * static_cast<uint64_t>(s.nq);
-    const uint64_t pieces = (bytes + kPrefetchBytes - 1) / kPrefetchBytes;
-    for (uint64_t i = tid; i < pieces; i += kThreads)
-      prefetch_l2(reinterpret_cast<const char*>(s.vec) + i * kPrefetchBytes,
-                  static_cast<uint32_t>(min(static_cast<uint64_t>(kPrefetchBytes),
-                                            bytes - i * kPrefetchBytes)));
-  }
+  // pull the whole slice towards L2; every pass below then reads L2. A sampled row
+  // does this once its sample has arrived (inside sample_lambda), so that the
+  // sample loads do not queue behind the bulk traffic of every row.
+  if (!sampled) prefetch_slice(s);
   if (G > 1)
     cluster_sync();  // all CTAs running; CTA 0's histograms and counters cleared
   else
@@ -1063,8 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   if (p.use_filter) {
     uint32_t shift2 = 0;
     const uint32_t lambda =
-        sampled ? sample_lambda(s, sm, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl,
-                                &shift2)
+        sampled ? sample_lambda(sm, s, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl, &shift2)
                 : 0u;
     if constexpr (F == kPaged) {
       if (pages > 0) {
@@ -1076,42 +1147,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         m.pt_smem = pt_smem;  // visible to all threads after the next barrier
       }
     }
-    // the candidate histogram: CTA 0's mhist when G > 1, else hist (cleared here)
-    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
-    if (G > 1) {
-      cluster_sync();  // CTA 0's mhist is zero again
-      Sink<true> rs;
-      rs.buf = buf;
-      rs.cnt = &ctl.cand_cnt;
-      rs.hist = mhist;
-      rs.buf_remote = map_rank(smem_addr(buf), 0);
-      rs.cnt_remote = map_rank(smem_addr(&ctl.cand_cnt), 0);
-      rs.hist_remote = map_rank(smem_addr(mhist), 0);
-      rs.cap = cap;
-      rs.lambda = lambda;
-      rs.shift = shift2;
-      if (lambda >= 0x80000000u)
-        filter_pass<true>(s, lambda, rs);
-      else
-        filter_pass<false>(s, lambda, rs);
-    } else {
-      __syncthreads();
-      Sink<false> ls;
-      ls.buf = buf;
-      ls.cnt = &ctl.cand_cnt;
-      ls.hist = hist;
-      ls.buf_remote = ls.cnt_remote = ls.hist_remote = 0u;
-      ls.cap = cap;
-      ls.lambda = lambda;
-      ls.shift = shift2;
-      if (lambda >= 0x80000000u)
-        filter_pass<true>(s, lambda, ls);
-      else
-        filter_pass<false>(s, lambda, ls);
-    }
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;  // the candidate histogram
+    const bool remote = G > 1 && rank != 0;
+    const uint32_t buf_remote = G > 1 ? map_rank(smem_addr(buf), 0) : 0u;
+    const uint32_t cnt_remote = G > 1 ? map_rank(smem_addr(&ctl.cand_cnt), 0) : 0u;
+    if (lambda >= 0x80000000u)
+      filter_positions<true>(s, lambda, buf, buf_remote, cnt_remote, remote, G > 1, cap, ctl);
+    else
+      filter_positions<false>(s, lambda, buf, buf_remote, cnt_remote, remote, G > 1, cap, ctl);
     uint32_t n_cand;
     if (G > 1) {
-      cluster_sync();  // every candidate is in CTA 0's buffer
+      cluster_sync();  // every candidate position is in CTA 0's buffer
       if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
       cluster_sync();
       n_cand = ctl.n_cand;
@@ -1120,13 +1166,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       n_cand = ctl.cand_cnt;
     }
     if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap) {
-      if (rank == 0)
-        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), G > 1 ? mhist : hist, lambda,
-                             shift2, list, hist, L, out, m, ctl);
+      if (rank == 0) {
+        fill_candidates(rowp, buf, n_cand, lambda, shift2, hist);
+        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), hist, lambda, shift2, list,
+                             hist, L, out, m, ctl);
+      }
       return;
     }
     // too few (lambda above the k-th key) or too many candidates: exact tier
-    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
     if (G > 1) {
       if (rank == 0)
         for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
