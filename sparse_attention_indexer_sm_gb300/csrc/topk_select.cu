@@ -65,7 +65,7 @@ constexpr int kFilterUnroll = 8;      // 128-bit loads in flight per thread in t
 constexpr int kMaskIters = 4;         // filter iterations whose masks are decoded together
 constexpr int kRowRoundBits = 12;     // histogram width of the rounds over the row
 constexpr int kBufRoundBits = 12;     // histogram width of the rounds over a buffer
-constexpr int kSampleQuads = 2;       // sampled 16-byte quads per thread
+constexpr int kSampleQuads = 1;       // sampled 16-byte quads per thread
 constexpr uint32_t kPrefetchBytes = 16384;  // one bulk L2 prefetch
 constexpr int kPtCap = 4096;          // page-table entries staged in shared memory
 constexpr int kRankDirect = 64;       // threshold bins this small are ordered by rank count
@@ -86,6 +86,7 @@ struct Ctl {
   uint32_t n_cand;                    // cand_cnt of CTA 0, broadcast
   uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
   uint32_t ns;                        // valid sample size (CTA 0)
+  uint32_t top_cnt;                   // candidates in the last candidate-histogram bin
   uint32_t gbase;                     // first buffer slot of the current filter group
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
@@ -572,13 +573,17 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
                                                   uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
   const int tid = threadIdx.x;
   // round 1: coarse bins (top 12 key bits); the valid sample size goes to CTA 0
+  // the sample keys crowd into a few coarse bins: one atomic per distinct bin per
+  // warp instruction
   uint32_t mine = 0;
 #pragma unroll
   for (int i = 0; i < 4 * kSampleQuads; ++i) {
-    if (sample_valid(sm, i, L)) {
-      atomicAdd(&hist[hist_index(static_cast<int>(sm.key[i] >> 20))], 1u);
-      ++mine;
-    }
+    const bool v = sample_valid(sm, i, L);
+    const uint32_t bin = v ? (sm.key[i] >> 20) : 0xFFFFFFFFu;
+    const uint32_t peers = __match_any_sync(kFull, bin);
+    if (v && (tid & 31) == __ffs(peers) - 1)
+      atomicAdd(&hist[hist_index(static_cast<int>(bin))], static_cast<uint32_t>(__popc(peers)));
+    mine += v ? 1u : 0u;
   }
   prefetch_slice(s);  // the sample has arrived: now the bulk of the slice
 #pragma unroll
@@ -712,6 +717,7 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
   int32_t ej;
   const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
   bool first = true;
+  uint32_t running = 0;  // candidates of this CTA so far (single-CTA rows)
   for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
     uint32_t mk[MI];
 #pragma unroll
@@ -743,10 +749,14 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     uint32_t total;
     const uint32_t off = block_excl_scan(n, ctl, &total);
     if (total != 0) {
-      if (tid == 0)
-        ctl.gbase = cluster_cnt ? dsmem_fetch_add(cnt_remote, total) : atomicAdd(&ctl.cand_cnt, total);
-      __syncthreads();
-      uint32_t slot = ctl.gbase + off;
+      uint32_t g0 = running;
+      if (cluster_cnt) {
+        if (tid == 0) ctl.gbase = dsmem_fetch_add(cnt_remote, total);
+        __syncthreads();
+        g0 = ctl.gbase;
+      }
+      running += total;
+      uint32_t slot = g0 + off;
       auto put = [&](int32_t j) {
         if (slot < cap) {
           if (remote)
@@ -770,17 +780,21 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     }
     first = false;
   }
+  if (!cluster_cnt && tid == 0) ctl.cand_cnt = running;
 }
 
 // F2 (CTA 0 only): the n buffered positions get their keys, read back (from L2)
-// in batches of four per thread, and the candidate histogram (bin = (key - lambda)
-// >> shift; the last bin is filled in by select_candidates) is counted in `chist`,
-// which is zero on entry.
+// in batches of four per thread, and the candidate histogram (bin = min((key -
+// lambda) >> shift, 4095)) is counted in `chist`, which is zero on entry. The last
+// bin collects most candidates, so it is counted per warp (ballot) rather than by
+// one shared atomic per candidate.
 __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, uint32_t n,
                                                 uint32_t lambda, uint32_t shift,
-                                                uint32_t* chist) {
+                                                uint32_t* chist, Ctl& ctl) {
   const int tid = threadIdx.x;
-  for (uint32_t i0 = tid; i0 < n; i0 += 4 * kThreads) {
+  // the loop bound is the same for every thread (the ballot below needs whole warps)
+  for (uint32_t base = 0; base < n; base += 4 * kThreads) {
+    const uint32_t i0 = base + static_cast<uint32_t>(tid);
     uint32_t bits[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -790,14 +804,19 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const uint32_t i = i0 + r * kThreads;
+      const uint32_t key = order_key(bits[r]);
+      const uint32_t d = (key - lambda) >> shift;
+      const bool top = i < n && d >= static_cast<uint32_t>(kMaxBins - 1);
       if (i < n) {
-        const uint32_t key = order_key(bits[r]);
         buf[i].x = key;
-        const uint32_t d = (key - lambda) >> shift;
-        if (d < static_cast<uint32_t>(kMaxBins - 1)) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+        if (!top) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
       }
+      const uint32_t b = __ballot_sync(kFull, top);
+      if ((tid & 31) == 0 && b != 0) atomicAdd(&ctl.top_cnt, static_cast<uint32_t>(__popc(b)));
     }
   }
+  __syncthreads();
+  if (tid == 0) chist[hist_index(kMaxBins - 1)] = ctl.top_cnt;
   __syncthreads();
 }
 
@@ -875,31 +894,46 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
                                                   int32_t L, int32_t* out, const OutMap& m,
                                                   Ctl& ctl) {
   const int tid = threadIdx.x;
-  {  // the last bin holds every candidate the other bins do not
-    uint32_t part = 0;
-    for (int i = tid; i < kMaxBins - 1; i += kThreads) part += chist[hist_index(i)];
-    const uint32_t counted = block_sum(part, ctl);
-    if (tid == 0) chist[hist_index(kMaxBins - 1)] = n - counted;
-    __syncthreads();
-  }
   find_threshold(chist, kMaxBins, k, ctl);
   const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
   if (ct > static_cast<uint32_t>(kListCap)) {
     select_in_buffer<F>(buf, n, k, 0ull, 64, L, out, static_cast<int32_t>(k), 0u, m, h, ctl);
     return;
   }
-  // candidates above the threshold bin are winners; the bin's go to the list
-  const uint32_t npad = (n + kThreads - 1) / kThreads * kThreads;
-  for (uint32_t i = tid; i < npad; i += kThreads) {
-    uint2 e = make_uint2(0, 0);
-    if (i < n) e = buf[i];
-    const uint32_t b = min((e.x - lambda) >> shift, static_cast<uint32_t>(kMaxBins - 1));
-    const bool win = i < n && b > t;
-    const bool tie = i < n && b == t;
-    const uint32_t ws = warp_reserve_bit(&ctl.win_cnt, win);
-    const uint32_t ts = warp_reserve_bit(&ctl.tie_cnt, tie);
-    if (win && ws < above) emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y));
-    if (tie && ts < ct) list[ts] = e;
+  // candidates above the threshold bin are winners; the bin's go to the list. Each
+  // thread takes entries tid, tid + kThreads, ...; one block-wide prefix count of
+  // (winners, ties), packed in one word, gives every slot.
+  constexpr int kPer = kTieCapMax / kThreads;
+  uint32_t cls = 0;  // bit 2r: winner, bit 2r+1: tie, for entry tid + r * kThreads
+  uint32_t nw = 0, nt = 0;
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
+    if (i < n) {
+      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kMaxBins - 1));
+      if (b > t) {
+        cls |= 1u << (2 * r);
+        ++nw;
+      } else if (b == t) {
+        cls |= 2u << (2 * r);
+        ++nt;
+      }
+    }
+  }
+  uint32_t total;
+  const uint32_t off = block_excl_scan(nw | (nt << 16), ctl, &total);
+  uint32_t ws = off & 0xFFFFu, ts = off >> 16;
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const uint32_t c = (cls >> (2 * r)) & 3u;
+    const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
+    if (c == 1u) {
+      if (ws < above) emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(buf[i].y));
+      ++ws;
+    } else if (c == 2u) {
+      if (ts < ct) list[ts] = buf[i];
+      ++ts;
+    }
   }
   __syncthreads();
   const uint32_t need = k - above;  // 1 <= need <= ct
@@ -1058,6 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     ctl.out_cnt = 0;
     ctl.cand_cnt = 0;
     ctl.ns = 0;
+    ctl.top_cnt = 0;
     ctl.lambda = 0;
     ctl.lambda_shift = 0;
   }
@@ -1167,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     }
     if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap) {
       if (rank == 0) {
-        fill_candidates(rowp, buf, n_cand, lambda, shift2, hist);
+        fill_candidates(rowp, buf, n_cand, lambda, shift2, hist, ctl);
         select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), hist, lambda, shift2, list,
                              hist, L, out, m, ctl);
       }

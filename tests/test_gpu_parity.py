@@ -289,3 +289,19 @@ def test_side_stream_and_repeatability(pkg):
     b = run_gpu(pkg, w)
     assert (np.sort(a, 1) == np.sort(b, 1)).all()
     assert_parity(w, a, check_rows=4)
+
+
+@pytest.mark.parametrize("split", [1, 2])
+def test_candidate_counts_off_block_multiples(pkg, split):
+    """Rows that keep every element (length within the candidate buffer) with
+    lengths just past multiples of the block size: the candidate passes must stay
+    warp-uniform however many candidates there are."""
+    lens = [1025, 1537, 2049, 2100, 2561, 3000, 3585, 4095, 4096]
+    stride = 4200
+    g = workloads.rng(900 + split)
+    scores = workloads.random_rows(g, len(lens), stride, "normal", dup=True)
+    seq = np.array(lens, np.int32)
+    w = workloads.Workload("off_block_multiples", "raw", 1024, scores, seq)
+    with settings(pkg, split=split):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
