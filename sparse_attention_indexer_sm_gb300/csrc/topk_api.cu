@@ -46,9 +46,8 @@ int row_split_setting() {
 // PR #37591 page splits a row over several blocks only for small batches of long
 // rows (section "关键源码片段", row_split: no split under 65536 elements, at most
 // 32 blocks, none when fewer than 4). Here a split costs no extra launch (the CTAs
-// of a cluster merge histograms in distributed shared memory), so the rule is:
-// double the split while the whole grid still fits in one wave of two resident
-// CTAs per SM and each CTA keeps at least 4096 elements.
+// of a cluster merge histograms in distributed shared memory); the rule below is
+// the measured one. row_len <= 0 means unknown: treated as long.
 int choose_split(int32_t batch, int64_t row_len, int sm_count) {
   const int forced = row_split_setting();
   if (forced >= 1) {
@@ -56,12 +55,18 @@ int choose_split(int32_t batch, int64_t row_len, int sm_count) {
     while (g * 2 <= forced && g * 2 <= topk_gb300::kMaxCluster) g *= 2;
     return g;
   }
+  // Rows up to 32768 elements run fastest on one CTA each: a cluster adds
+  // barriers and distributed-shared-memory traffic that a slice this short does
+  // not pay back. Longer rows get about 8192 elements per CTA, as long as the
+  // grid still fits two CTAs per SM; two-CTA clusters measured slower than one
+  // CTA, so a split is at least four.
+  if (row_len > 0 && row_len <= 32768) return 1;
+  const int64_t len = row_len > 0 ? row_len : INT64_C(1) << 30;
   const int64_t slots = static_cast<int64_t>(sm_count) * 2;
   int g = 1;
-  while (g < topk_gb300::kMaxCluster && static_cast<int64_t>(batch) * g * 2 <= slots &&
-         (row_len <= 0 || row_len / (g * 2) >= 4096))
-    g *= 2;
-  return g;
+  while (g < topk_gb300::kMaxCluster && len / (g * 2) >= 8192) g *= 2;
+  while (g > 1 && static_cast<int64_t>(batch) * g > slots) g /= 2;
+  return g >= 4 ? g : 1;
 }
 
 int fail_cuda(cudaError_t e) {

@@ -13,20 +13,25 @@
 //  F1. sample    each CTA loads a strided sample of its slice (one 16-byte quad
 //                in every `stride` >= 8) before anything else. Two sample ranks are
 //                wanted: r_s, a few standard deviations below the expected sample rank
-//                of the row's k-th key, and r_lo as far above it. A 4096-bin histogram
-//                of the top 12 key bits (summed over the cluster through distributed
-//                shared memory) finds the coarse bins of both; a second 4096-bin
+//                of the row's k-th key, and r_lo as far above it. A 1024-bin histogram
+//                of the top 10 key bits (summed over the cluster through distributed
+//                shared memory) finds the coarse bins of both; a second 1024-bin
 //                histogram spanning just those coarse bins resolves them: lambda is the
-//                lower edge of r_s's fine bin, lambda_hi the upper edge of r_lo's. Rows
-//                that fit the candidate buffer skip the sample (lambda = 0).
+//                lower edge of r_s's fine bin, lambda_hi the upper edge of r_lo's. One
+//                warp finds each threshold. Rows that fit the candidate buffer skip the
+//                sample (lambda = 0).
 //  F2. filter    one streaming pass with 128-bit loads compares every raw fp32 bit
 //                pattern with lambda (a single integer compare: for lambda in the
 //                non-negative range a signed compare, otherwise an unsigned one,
-//                both equal to "key >= lambda"); candidates go, as (key, position),
-//                to CTA 0's shared buffer and into CTA 0's candidate histogram, whose
-//                4096 bins of width 2^s2 start at lambda (s2 chosen so that about
-//                2048 bins span [lambda, lambda_hi]; the last bin takes every larger
-//                key).
+//                both equal to "key >= lambda"). Candidates go to CTA 0's shared
+//                buffer as (key, position) and are counted in a 1024-bin candidate
+//                histogram whose bins of width 2^s2 start at lambda (s2 chosen so that
+//                fewer than 512 bins span [lambda, lambda_hi]; the last bin takes
+//                every larger key; rows that skip the sample use the top 10 key bits).
+//                A row owned by one CTA keeps only positions in the pass (so the
+//                loads of several iterations stay in flight) and reads the candidates'
+//                values back from L2 afterwards; the CTAs of a cluster write keys and
+//                their own histograms directly, summed into CTA 0's afterwards.
 //  F3. select    if the cluster found between k and capacity candidates, every
 //                element of the exact top-k is among them (they hold k elements with
 //                key >= lambda, so the k-th key is >= lambda). CTA 0 finds the
@@ -78,6 +83,18 @@ __host__ __device__ constexpr int hist_index(int b) { return b + (b >> 5); }
 constexpr int kHistWords = hist_index(kMaxBins);
 constexpr int kListCap = kHistWords / 2;  // (key, position) entries of the list region
 
+// The fast tier's histograms have 1024 bins, small enough for one warp to find a
+// threshold in (no block-wide scan). Each has its own region of `hist` (and, in
+// CTA 0 of a cluster, of `mhist`), all cleared once at the start: the sample's
+// coarse and fine rounds and the candidate histogram.
+constexpr int kFastBits = 10;
+constexpr int kFastBins = 1 << kFastBits;
+constexpr int kFastWords = hist_index(kFastBins);
+constexpr int kH1 = 0;                // sample, coarse round
+constexpr int kH2 = kFastWords;       // sample, fine round
+constexpr int kHC = 2 * kFastWords;   // candidates
+static_assert(3 * kFastWords <= kHistWords, "fast-tier histograms must fit the histogram region");
+
 struct Ctl {
   uint32_t scan[kWarps];              // per-warp partials of block scans
   uint32_t sel_t, sel_above, sel_count;  // threshold bin of the current round
@@ -87,7 +104,6 @@ struct Ctl {
   uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
   uint32_t ns;                        // valid sample size (CTA 0)
   uint32_t top_cnt;                   // candidates in the last candidate-histogram bin
-  uint32_t gbase;                     // first buffer slot of the current filter group
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
@@ -296,58 +312,56 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
   __syncthreads();
 }
 
-// Two thresholds of one histogram in one scan: need1 -> ctl.sel_*, need2 ->
-// ctl.sel2_* (both need <= sum of h).
-__device__ __forceinline__ void find_threshold2(const uint32_t* h, int nbins, uint32_t need1,
-                                                uint32_t need2, Ctl& ctl) {
-  constexpr int kMaxPer = kMaxBins / kThreads;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = nbins >= kThreads ? nbins / kThreads : 1;
-  const int b0 = tid * per;
-  uint32_t c[kMaxPer];
+// One warp (all 32 lanes) finds, in the padded kFastBins-bin histogram h, the
+// threshold bin for need1 (-> ctl.sel_*) and, if `two`, for need2 (-> ctl.sel2_*):
+// the bin where the count from the top reaches need (1 <= need <= sum of h). Lane
+// l first sums bins [32 l, 32 l + 32) (reads of 32 distinct banks, padded layout);
+// a suffix scan over the lanes names the lane whose range holds the threshold, and
+// the warp then scans that lane's 32 bins, one per lane. The results are visible
+// to the block after the caller's next barrier.
+__device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, uint32_t need2,
+                                           bool two, Ctl& ctl) {
+  const int lane = threadIdx.x & 31;
   uint32_t s = 0;
 #pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    c[i] = (i < per && b0 + i < nbins) ? h[hist_index(b0 + i)] : 0u;
-    s += c[i];
-  }
-  uint32_t x = s;
+  for (int i = 0; i < 32; ++i) s += h[hist_index(lane * 32 + i)];
+  uint32_t x = s;  // count in the bins of lanes >= lane
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const uint32_t y = __shfl_down_sync(kFull, x, off);
     if (lane + off < 32) x += y;
   }
-  if (lane == 0) ctl.scan[warp] = x;
-  __syncthreads();
-  uint32_t higher = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) higher += w > warp ? ctl.scan[w] : 0u;
-  const uint32_t excl = higher + x - s;
+  const uint32_t excl = x - s;  // count in the bins of lanes > lane
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
+    if (q == 1 && !two) break;
     const uint32_t need = q == 0 ? need1 : need2;
-    if (s != 0 && excl < need && need <= excl + s) {
-      uint32_t acc = excl;
-      bool found = false;
+    const uint32_t hit = __ballot_sync(kFull, s != 0 && excl < need && need <= x);
+    if (hit == 0u) continue;  // need outside [1, sum]: nothing to find
+    const int owner = __ffs(hit) - 1;
+    const uint32_t owner_above = __shfl_sync(kFull, excl, owner);
+    const int b = owner * 32 + lane;
+    const uint32_t c = h[hist_index(b)];
+    uint32_t y = c;  // count in the owner's bins >= b
 #pragma unroll
-      for (int i = kMaxPer - 1; i >= 0; --i) {
-        if (!found && i < per && acc + c[i] >= need) {
-          if (q == 0) {
-            ctl.sel_t = static_cast<uint32_t>(b0 + i);
-            ctl.sel_above = acc;
-            ctl.sel_count = c[i];
-          } else {
-            ctl.sel2_t = static_cast<uint32_t>(b0 + i);
-            ctl.sel2_above = acc;
-            ctl.sel2_count = c[i];
-          }
-          found = true;
-        }
-        acc += found ? 0u : c[i];
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t z = __shfl_down_sync(kFull, y, off);
+      if (lane + off < 32) y += z;
+    }
+    const uint32_t above = owner_above + y - c;
+    const uint32_t here = __ballot_sync(kFull, c != 0 && above < need && need <= above + c);
+    if (here != 0u && lane == __ffs(here) - 1) {
+      if (q == 0) {
+        ctl.sel_t = static_cast<uint32_t>(b);
+        ctl.sel_above = above;
+        ctl.sel_count = c;
+      } else {
+        ctl.sel2_t = static_cast<uint32_t>(b);
+        ctl.sel2_above = above;
+        ctl.sel2_count = c;
       }
     }
   }
-  __syncthreads();
 }
 
 // Cluster-wide threshold bin of the CTAs' histograms `hist` (complete and
@@ -554,35 +568,37 @@ __device__ __forceinline__ bool sample_valid(const Sample& sm, int i, int32_t L)
   return sm.j[i / 4] < L - (i & 3);
 }
 
-// Sums this CTA's histogram into CTA 0's `mhist` (G > 1; cluster barrier after).
-__device__ __forceinline__ void merge_into_cta0(const uint32_t* hist, uint32_t* mhist) {
-  const uint32_t m0 = map_rank(smem_addr(mhist), 0);
-  for (int i = threadIdx.x; i < kHistWords; i += kThreads) {
-    const uint32_t v = hist[i];
+// Sums the `words` words of this CTA's histogram region h into the same region of
+// CTA 0 (mh, G > 1), then a cluster barrier.
+__device__ __forceinline__ void merge_into_cta0(const uint32_t* h, uint32_t* mh, int words) {
+  const uint32_t m0 = map_rank(smem_addr(mh), 0);
+  for (int i = threadIdx.x; i < words; i += kThreads) {
+    const uint32_t v = h[i];
     if (v != 0) dsmem_add(m0 + 4u * static_cast<uint32_t>(i), v);
   }
   cluster_sync();
 }
 
 // F1b: lambda and the candidate-histogram bin width from the cluster's sample (see
-// the header comment). `hist`, CTA 0's `mhist` and CTA 0's ctl.ns are zero on
-// entry; on return `hist` holds garbage and `mhist` is zero. Returns lambda;
-// *shift2 gets the candidate-histogram bin width exponent.
+// the header comment). The kH1 and kH2 regions of `hist` and of CTA 0's `mhist`
+// are zero on entry, and so is CTA 0's ctl.ns. Returns lambda; *shift2 gets the
+// candidate-histogram bin width exponent.
 __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice& s, int32_t L,
                                                   uint32_t k, int G, int rank, uint32_t* hist,
                                                   uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
   const int tid = threadIdx.x;
-  // round 1: coarse bins (top 12 key bits); the valid sample size goes to CTA 0
-  // the sample keys crowd into a few coarse bins: one atomic per distinct bin per
-  // warp instruction
+  const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
+  // round 1: coarse bins (top 10 key bits); the sample keys crowd into a few bins,
+  // so one atomic per distinct bin per warp instruction. The valid sample size
+  // goes to CTA 0.
   uint32_t mine = 0;
 #pragma unroll
   for (int i = 0; i < 4 * kSampleQuads; ++i) {
     const bool v = sample_valid(sm, i, L);
-    const uint32_t bin = v ? (sm.key[i] >> 20) : 0xFFFFFFFFu;
+    const uint32_t bin = v ? (sm.key[i] >> (32 - kFastBits)) : 0xFFFFFFFFu;
     const uint32_t peers = __match_any_sync(kFull, bin);
     if (v && (tid & 31) == __ffs(peers) - 1)
-      atomicAdd(&hist[hist_index(static_cast<int>(bin))], static_cast<uint32_t>(__popc(peers)));
+      atomicAdd(&hist[kH1 + hist_index(static_cast<int>(bin))], static_cast<uint32_t>(__popc(peers)));
     mine += v ? 1u : 0u;
   }
   prefetch_slice(s);  // the sample has arrived: now the bulk of the slice
@@ -595,11 +611,11 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
       dsmem_add(map_rank(smem_addr(&ctl.ns), 0), mine);
   }
   __syncthreads();
-  if (G > 1) merge_into_cta0(hist, mhist);
+  if (G > 1) merge_into_cta0(hist + kH1, mhist + kH1, kFastWords);
   // sample ranks a few standard deviations either side of the expected sample rank
-  // of the row's k-th key (CTA 0 only)
+  // of the row's k-th key
   uint32_t rs = 0, rs_lo = 0;
-  if (rank == 0) {
+  if (finder) {
     const uint32_t ns = ctl.ns;
     if (ns != 0) {
       const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
@@ -609,35 +625,33 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
       const float lo = floorf(mean - dev);
       rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
       if (rs_lo > rs) rs_lo = rs;
-      find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs, rs_lo, ctl);
+      warp_find2((G > 1 ? mhist : hist) + kH1, rs, rs_lo, true, ctl);
     }
+    __syncwarp();
     if (tid == 0) {
+      constexpr int kC = 32 - kFastBits;  // coarse bin width exponent
       if (ns != 0) {
-        // fine window: coarse bins sel_t .. sel2_t, at most 4096 fine bins
-        const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1 - ctl.sel_t) << 20;
-        const int f = max(0, (64 - __clzll(static_cast<long long>(span - 1))) - 12);
-        ctl.win_lo = ctl.sel_t << 20;
+        // fine window: coarse bins sel_t .. sel2_t in at most kFastBins fine bins
+        const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1 - ctl.sel_t) << kC;
+        const int f = max(0, (64 - __clzll(static_cast<long long>(span - 1))) - kFastBits);
+        ctl.win_lo = ctl.sel_t << kC;
         ctl.win_shift = static_cast<uint32_t>(f);
         ctl.win_above = ctl.sel2_above;  // sample keys above the window
-      } else {  // no sample below the row's length: keep everything
+      } else {  // no sample below the row's length: an empty window, lambda = 0
         ctl.sel2_t = 0;
         ctl.win_lo = 0;
-        ctl.win_shift = 8;
+        ctl.win_shift = kC;
         ctl.win_above = 0;
       }
     }
-    if (G > 1) {
-      __syncthreads();
-      if (tid > 0 && tid < G) {
-        dsmem_st(map_rank(smem_addr(&ctl.win_lo), tid), ctl.win_lo);
-        dsmem_st(map_rank(smem_addr(&ctl.win_shift), tid), ctl.win_shift);
-        dsmem_st(map_rank(smem_addr(&ctl.win_above), tid), ctl.win_above);
-        dsmem_st(map_rank(smem_addr(&ctl.sel2_t), tid), ctl.sel2_t);
-      }
-      for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+    __syncwarp();
+    if (G > 1 && tid > 0 && tid < G) {
+      dsmem_st(map_rank(smem_addr(&ctl.win_lo), tid), ctl.win_lo);
+      dsmem_st(map_rank(smem_addr(&ctl.win_shift), tid), ctl.win_shift);
+      dsmem_st(map_rank(smem_addr(&ctl.win_above), tid), ctl.win_above);
+      dsmem_st(map_rank(smem_addr(&ctl.sel2_t), tid), ctl.sel2_t);
     }
   }
-  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
   if (G > 1)
     cluster_sync();
   else
@@ -645,38 +659,39 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
 
   // round 2: fine bins over [win_lo, end of coarse bin sel2_t]
   const uint32_t win_lo = ctl.win_lo, f = ctl.win_shift, win_above = ctl.win_above;
-  const uint64_t span = static_cast<uint64_t>(ctl.sel2_t + 1) * (1ull << 20) - win_lo;
+  const uint64_t span =
+      (static_cast<uint64_t>(ctl.sel2_t + 1) << (32 - kFastBits)) - static_cast<uint64_t>(win_lo);
 #pragma unroll
   for (int i = 0; i < 4 * kSampleQuads; ++i) {
     const uint64_t d = static_cast<uint64_t>(sm.key[i]) - win_lo;  // wraps for keys below
     if (sample_valid(sm, i, L) && sm.key[i] >= win_lo && d < span)
-      atomicAdd(&hist[hist_index(static_cast<int>(d >> f))], 1u);
+      atomicAdd(&hist[kH2 + hist_index(static_cast<int>(d >> f))], 1u);
   }
   __syncthreads();
-  if (G > 1) merge_into_cta0(hist, mhist);
-  if (rank == 0) {
-    if (rs != 0) find_threshold2(G > 1 ? mhist : hist, kMaxBins, rs - win_above, rs_lo - win_above, ctl);
+  if (G > 1) merge_into_cta0(hist + kH2, mhist + kH2, kFastWords);
+  if (finder) {
+    if (rs != 0)
+      warp_find2((G > 1 ? mhist : hist) + kH2, rs - win_above, rs_lo - win_above, true, ctl);
+    __syncwarp();
     if (tid == 0) {
       if (rs != 0) {
+        // [lambda, lambda_hi] spans fewer than 512 candidate bins
         const uint32_t lam = win_lo + (ctl.sel_t << f);
         const uint64_t hi =
             static_cast<uint64_t>(win_lo) + (static_cast<uint64_t>(ctl.sel2_t + 1) << f) - 1;
         const uint64_t gap = hi > lam ? hi - lam : 0;
         const int bits = 64 - __clzll(static_cast<long long>(gap));
         ctl.lambda = lam;
-        ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - 11));
+        ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - (kFastBits - 1)));
       } else {
         ctl.lambda = 0;
-        ctl.lambda_shift = 20;
+        ctl.lambda_shift = 32 - kFastBits;
       }
     }
-    if (G > 1) {
-      __syncthreads();
-      if (tid > 0 && tid < G) {
-        dsmem_st(map_rank(smem_addr(&ctl.lambda), tid), ctl.lambda);
-        dsmem_st(map_rank(smem_addr(&ctl.lambda_shift), tid), ctl.lambda_shift);
-      }
-      for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+    __syncwarp();
+    if (G > 1 && tid > 0 && tid < G) {
+      dsmem_st(map_rank(smem_addr(&ctl.lambda), tid), ctl.lambda);
+      dsmem_st(map_rank(smem_addr(&ctl.lambda_shift), tid), ctl.lambda_shift);
     }
   }
   if (G > 1)
@@ -698,17 +713,15 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
     return bits <= thr;
 }
 
-// F2: stream the slice, keep per lane a 32-bit candidate mask per iteration (8
-// quads), and every kMaskIters iterations turn the masks into positions written
-// compactly into CTA 0's buffer (entry .y; .x is filled by fill_candidates). The
-// slots come from one block-wide prefix count per group and one reservation on
-// CTA 0's counter per group (a distributed-shared-memory atomic in every CTA when
-// the cluster has several). Slots at or beyond `cap` are counted but not written.
+// F2, a row owned by one CTA: stream the row, keep per lane a 32-bit candidate
+// mask per iteration (8 quads), and every kMaskIters iterations turn the masks into
+// positions written compactly into the buffer (entry .y; .x is filled by
+// fill_candidates) at slots from one block-wide prefix count per group. Holding
+// only masks lets the loads of a whole group be in flight together. Slots at or
+// beyond `cap` are counted but not written.
 template <bool kPos>
 __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint2* buf,
-                                                 uint32_t buf_remote, uint32_t cnt_remote,
-                                                 bool remote, bool cluster_cnt, uint32_t cap,
-                                                 Ctl& ctl) {
+                                                 uint32_t cap, Ctl& ctl) {
   const int tid = threadIdx.x;
   const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
   constexpr int U = kFilterUnroll;
@@ -717,7 +730,7 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
   int32_t ej;
   const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
   bool first = true;
-  uint32_t running = 0;  // candidates of this CTA so far (single-CTA rows)
+  uint32_t running = 0;  // candidates so far
   for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
     uint32_t mk[MI];
 #pragma unroll
@@ -749,21 +762,10 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     uint32_t total;
     const uint32_t off = block_excl_scan(n, ctl, &total);
     if (total != 0) {
-      uint32_t g0 = running;
-      if (cluster_cnt) {
-        if (tid == 0) ctl.gbase = dsmem_fetch_add(cnt_remote, total);
-        __syncthreads();
-        g0 = ctl.gbase;
-      }
+      uint32_t slot = running + off;
       running += total;
-      uint32_t slot = g0 + off;
       auto put = [&](int32_t j) {
-        if (slot < cap) {
-          if (remote)
-            dsmem_st(buf_remote + 8u * slot + 4u, static_cast<uint32_t>(j));
-          else
-            buf[slot].y = static_cast<uint32_t>(j);
-        }
+        if (slot < cap) buf[slot].y = static_cast<uint32_t>(j);
         ++slot;
       };
       if (with_edge) put(ej);
@@ -780,12 +782,13 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     }
     first = false;
   }
-  if (!cluster_cnt && tid == 0) ctl.cand_cnt = running;
+  if (tid == 0) ctl.cand_cnt = running;
 }
 
-// F2 (CTA 0 only): the n buffered positions get their keys, read back (from L2)
-// in batches of four per thread, and the candidate histogram (bin = min((key -
-// lambda) >> shift, 4095)) is counted in `chist`, which is zero on entry. The last
+// F2, a row owned by one CTA: the n buffered positions get their keys, read back
+// (from L2) in batches of four per thread, and the candidate histogram (bin =
+// min((key - lambda) >> shift, kFastBins - 1)) is counted in `chist`, which is zero
+// on entry. The last
 // bin collects most candidates, so it is counted per warp (ballot) rather than by
 // one shared atomic per candidate.
 __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, uint32_t n,
@@ -806,7 +809,7 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
       const uint32_t i = i0 + r * kThreads;
       const uint32_t key = order_key(bits[r]);
       const uint32_t d = (key - lambda) >> shift;
-      const bool top = i < n && d >= static_cast<uint32_t>(kMaxBins - 1);
+      const bool top = i < n && d >= static_cast<uint32_t>(kFastBins - 1);
       if (i < n) {
         buf[i].x = key;
         if (!top) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
@@ -816,8 +819,84 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
     }
   }
   __syncthreads();
-  if (tid == 0) chist[hist_index(kMaxBins - 1)] = ctl.top_cnt;
+  if (tid == 0) chist[hist_index(kFastBins - 1)] = ctl.top_cnt;
   __syncthreads();
+}
+
+// F2, a row split over a cluster: stream the slice; every element with key >=
+// lambda goes, as (key, position), to CTA 0's buffer and into this CTA's candidate
+// histogram `chist` (bin = min((key - lambda) >> shift, kFastBins - 1); zero on
+// entry), so
+// that CTA 0 does not have to read the keys back for the whole row. Slots come
+// from one reservation per warp and iteration on CTA 0's counter through
+// distributed shared memory; slots at or beyond `cap` are counted but not written.
+// The last bin, which takes most candidates, is counted per lane and added once
+// per warp. `remote`: this CTA is not CTA 0.
+template <bool kPos>
+__device__ __forceinline__ void filter_candidates(const Slice& s, uint32_t lambda, uint32_t shift,
+                                                  uint2* buf, uint32_t buf_remote,
+                                                  uint32_t cnt_remote, bool remote, uint32_t cap,
+                                                  uint32_t* chist, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
+  constexpr int U = kFilterUnroll;
+  constexpr int32_t kStep = U * kThreads;
+  uint32_t top = 0;
+  auto put = [&](uint32_t slot, uint32_t bits, int32_t j) {
+    const uint32_t key = order_key(bits);
+    const uint32_t d = (key - lambda) >> shift;
+    if (d >= static_cast<uint32_t>(kFastBins - 1))
+      ++top;
+    else
+      atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+    if (slot < cap) {
+      if (remote)
+        dsmem_st2(buf_remote + 8u * slot, key, static_cast<uint32_t>(j));
+      else
+        buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
+    }
+  };
+  {  // the unaligned head/tail element of this thread, if any
+    int32_t ej;
+    const bool e = edge_position(s, &ej);
+    const uint32_t bits = e ? __float_as_uint(s.row[ej]) : 0u;
+    const bool c = e && is_candidate<kPos>(bits, thr);
+    const uint32_t slot = warp_reserve(&ctl.cand_cnt, cnt_remote, true, c ? 1u : 0u);
+    if (c) put(slot, bits, ej);
+  }
+  for (int32_t base = 0; base < s.nq; base += kStep) {
+    uint4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t q = base + u * kThreads + tid;
+      x[u] = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool ok = base + u * kThreads + tid < s.nq;
+      m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].x, thr)) << (4 * u + 0);
+      m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].y, thr)) << (4 * u + 1);
+      m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].z, thr)) << (4 * u + 2);
+      m |= static_cast<uint32_t>(ok && is_candidate<kPos>(x[u].w, thr)) << (4 * u + 3);
+    }
+    uint32_t slot = warp_reserve(&ctl.cand_cnt, cnt_remote, true,
+                                 static_cast<uint32_t>(__popc(m)));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint32_t nib = (m >> (4 * u)) & 15u;
+      const int32_t j = s.j0 + 4 * (base + u * kThreads + tid);
+      while (nib != 0u) {
+        const int c = __ffs(nib) - 1;
+        nib &= nib - 1u;
+        const uint32_t bits = c == 0 ? x[u].x : c == 1 ? x[u].y : c == 2 ? x[u].z : x[u].w;
+        put(slot++, bits, j + c);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
+  if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kFastBins - 1)], top);
 }
 
 // ------------------------------------------------------------------ selection in a buffer
@@ -884,7 +963,7 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
 }
 
 // F3 (CTA 0 only): the filter left n candidates in buf and their histogram (bin =
-// min((key - lambda) >> shift, 4095)) in chist. Writes the k largest composites
+// min((key - lambda) >> shift, kFastBins - 1)) in chist. Writes the k largest composites
 // (key, ~position) mapped to out. h may be chist itself: it is used only after
 // chist has been read.
 template <int F>
@@ -894,7 +973,8 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
                                                   int32_t L, int32_t* out, const OutMap& m,
                                                   Ctl& ctl) {
   const int tid = threadIdx.x;
-  find_threshold(chist, kMaxBins, k, ctl);
+  if (tid < 32) warp_find2(chist, k, 0u, false, ctl);
+  __syncthreads();
   const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
   if (ct > static_cast<uint32_t>(kListCap)) {
     select_in_buffer<F>(buf, n, k, 0ull, 64, L, out, static_cast<int32_t>(k), 0u, m, h, ctl);
@@ -910,7 +990,7 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
   for (int r = 0; r < kPer; ++r) {
     const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
     if (i < n) {
-      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kMaxBins - 1));
+      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kFastBins - 1));
       if (b > t) {
         cls |= 1u << (2 * r);
         ++nw;
@@ -1168,7 +1248,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   // ---------------- fast tier
   if (p.use_filter) {
-    uint32_t shift2 = 0;
+    uint32_t shift2 = 32 - kFastBits;  // rows that skip the sample: the top key bits
     const uint32_t lambda =
         sampled ? sample_lambda(sm, s, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl, &shift2)
                 : 0u;
@@ -1182,33 +1262,41 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         m.pt_smem = pt_smem;  // visible to all threads after the next barrier
       }
     }
-    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;  // the candidate histogram
-    const bool remote = G > 1 && rank != 0;
-    const uint32_t buf_remote = G > 1 ? map_rank(smem_addr(buf), 0) : 0u;
-    const uint32_t cnt_remote = G > 1 ? map_rank(smem_addr(&ctl.cand_cnt), 0) : 0u;
-    if (lambda >= 0x80000000u)
-      filter_positions<true>(s, lambda, buf, buf_remote, cnt_remote, remote, G > 1, cap, ctl);
-    else
-      filter_positions<false>(s, lambda, buf, buf_remote, cnt_remote, remote, G > 1, cap, ctl);
     uint32_t n_cand;
-    if (G > 1) {
-      cluster_sync();  // every candidate position is in CTA 0's buffer
-      if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
-      cluster_sync();
-      n_cand = ctl.n_cand;
-    } else {
+    uint32_t* chist = hist + kHC;
+    if (G == 1) {
+      if (lambda >= 0x80000000u)
+        filter_positions<true>(s, lambda, buf, cap, ctl);
+      else
+        filter_positions<false>(s, lambda, buf, cap, ctl);
       __syncthreads();
       n_cand = ctl.cand_cnt;
+      if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
+        fill_candidates(rowp, buf, n_cand, lambda, shift2, chist, ctl);
+    } else {
+      const bool remote = rank != 0;
+      const uint32_t buf_remote = map_rank(smem_addr(buf), 0);
+      const uint32_t cnt_remote = map_rank(smem_addr(&ctl.cand_cnt), 0);
+      if (lambda >= 0x80000000u)
+        filter_candidates<true>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap, chist,
+                                ctl);
+      else
+        filter_candidates<false>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap,
+                                 chist, ctl);
+      cluster_sync();  // every candidate is in CTA 0's buffer; the counter is final
+      if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
+      merge_into_cta0(chist, mhist + kHC, kFastWords);  // ends with a cluster barrier
+      n_cand = ctl.n_cand;
+      chist = mhist + kHC;
     }
     if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap) {
-      if (rank == 0) {
-        fill_candidates(rowp, buf, n_cand, lambda, shift2, hist, ctl);
-        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), hist, lambda, shift2, list,
+      if (rank == 0)
+        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
                              hist, L, out, m, ctl);
-      }
       return;
     }
     // too few (lambda above the k-th key) or too many candidates: exact tier
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
     if (G > 1) {
       if (rank == 0)
         for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
