@@ -187,6 +187,17 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
+// Asynchronous 4-byte copy global -> shared (no register holds the value).
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
+// Waits until this thread's asynchronous copies have landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Ask the memory system to bring [p, p + bytes) into L2 (16-byte aligned, bytes a
 // multiple of 16). Nothing waits for it; later loads simply hit L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
@@ -1221,20 +1232,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const Slice s = make_slice(rowp, L, rank, G);
   const bool sampled = p.use_filter && static_cast<uint32_t>(L) > cap;
   if (sampled && !sample_loaded) load_sample(s, sm);
-  // paged: the row's page table is read now (into registers) and staged in shared
-  // memory after the sample, when the loads have long completed
-  constexpr int kPtPer = kPtCap / kThreads;
-  int32_t pt_reg[F == kPaged ? kPtPer : 1];
+  // paged: CTA 0, which writes the fast tier's output, copies the row's page table
+  // to shared memory asynchronously (waited for after the sample); the other CTAs
+  // of a cluster, and rows of more than kPtCap pages, read it from global memory
   int32_t pages = 0;
   if constexpr (F == kPaged) {
     const int64_t np = (static_cast<int64_t>(L) + p.page_size - 1) / p.page_size;
-    if (np <= kPtCap) {
+    if (rank == 0 && np <= kPtCap) {
       pages = static_cast<int32_t>(np);
-#pragma unroll
-      for (int r = 0; r < kPtPer; ++r) {
-        const int32_t i = tid + r * kThreads;
-        pt_reg[r] = i < pages ? __ldg(m.pt_row + i) : 0;
-      }
+      for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, m.pt_row + i);
     }
   }
   // pull the whole slice towards L2; every pass below then reads L2. A sampled row
@@ -1254,11 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
                 : 0u;
     if constexpr (F == kPaged) {
       if (pages > 0) {
-#pragma unroll
-        for (int r = 0; r < kPtPer; ++r) {
-          const int32_t i = tid + r * kThreads;
-          if (i < pages) pt_smem[i] = pt_reg[r];
-        }
+        cp_async_wait_all();
         m.pt_smem = pt_smem;  // visible to all threads after the next barrier
       }
     }
@@ -1308,12 +1310,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
   if constexpr (F == kPaged) {
-    if (pages > 0 && m.pt_smem == nullptr) {
-#pragma unroll
-      for (int r = 0; r < kPtPer; ++r) {
-        const int32_t i = tid + r * kThreads;
-        if (i < pages) pt_smem[i] = pt_reg[r];
-      }
+    if (pages > 0 && m.pt_smem == nullptr) {  // the fast tier did not run
+      cp_async_wait_all();
       __syncthreads();
       m.pt_smem = pt_smem;
     }
