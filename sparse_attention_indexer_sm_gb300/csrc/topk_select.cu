@@ -10,10 +10,10 @@
 // overflows. On this machine it runs in two tiers:
 //
 // Fast tier (one pass over the row, normally the only one):
-//  F1. sample    each CTA loads a strided sample of its slice (one 16-byte quad
-//                in every `stride` >= 8) before anything else. Two sample ranks are
-//                wanted: r_s, a few standard deviations below the expected sample rank
-//                of the row's k-th key, and r_lo as far above it. A 1024-bin histogram
+//  F1. sample    each CTA loads a sample of its slice (one 16-byte quad per thread,
+//                in runs of 512 bytes) before anything else. Two sample ranks are
+//                wanted: r_s, four standard deviations below the expected sample rank
+//                of the row's k-th key, and r_lo three above it. A 1024-bin histogram
 //                of the top 10 key bits (summed over the cluster through distributed
 //                shared memory) finds the coarse bins of both; a second 1024-bin
 //                histogram spanning just those coarse bins resolves them: lambda is the
@@ -546,7 +546,7 @@ __device__ __forceinline__ void emit(int32_t* out, int32_t k, uint32_t slot, con
 
 // ------------------------------------------------------------------ fast tier
 
-// F1a: the strided sample of a CTA's part of the row: keys of the sampled 16-byte
+// F1a: the sample of a CTA's part of the row: keys of the sampled 16-byte
 // quads and the row position of each quad's first element (INT32_MAX when the
 // thread has no quad). An element counts only if its position is below the row's
 // length, which for the raw and paged forms is read while the sample is in flight.
@@ -555,16 +555,17 @@ struct Sample {
   int32_t j[kSampleQuads];
 };
 
-__device__ __forceinline__ int32_t sample_stride(int32_t nq) {
-  const int32_t per = kThreads * kSampleQuads;
-  return max(8, (nq + per - 1) / per);
-}
-
+// The sample is taken in runs of 32 consecutive quads (512 bytes, one per warp and
+// round) spread evenly over the slice: whole DRAM bursts instead of one 16-byte
+// piece of every few lines, so the sample arrives sooner; the later stream finds
+// these lines in L2.
 __device__ __forceinline__ void load_sample(const Slice& s, Sample& sm) {
-  const int32_t stride = sample_stride(s.nq);
+  constexpr int32_t kRuns = kWarps * kSampleQuads;
+  const int32_t spacing = max(32, s.nq / kRuns);  // quads from one run to the next
 #pragma unroll
   for (int r = 0; r < kSampleQuads; ++r) {
-    const int32_t q = (static_cast<int32_t>(threadIdx.x) + r * kThreads) * stride;
+    const int32_t run = static_cast<int32_t>(threadIdx.x >> 5) + r * kWarps;
+    const int32_t q = run * spacing + static_cast<int32_t>(threadIdx.x & 31);
     const bool ok = q < s.nq;
     const uint4 x = ok ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
     sm.key[4 * r + 0] = order_key(x.x);
@@ -629,11 +630,14 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   if (finder) {
     const uint32_t ns = ctl.ns;
     if (ns != 0) {
+      // four standard deviations on lambda's side (a lambda above the k-th key
+      // costs the exact tier: about 3e-5 of rows), three on the other (it only sets
+      // the candidate-histogram bin width)
       const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
-      const float dev = 3.0f * sqrtf(mean);
-      rs = static_cast<uint32_t>(ceilf(mean + dev)) + 2u;
+      const float sd = sqrtf(mean);
+      rs = static_cast<uint32_t>(ceilf(mean + 4.0f * sd)) + 2u;
       if (rs > ns) rs = ns;
-      const float lo = floorf(mean - dev);
+      const float lo = floorf(mean - 3.0f * sd);
       rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
       if (rs_lo > rs) rs_lo = rs;
       warp_find2((G > 1 ? mhist : hist) + kH1, rs, rs_lo, true, ctl);
