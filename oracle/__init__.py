@@ -78,6 +78,9 @@ class Oracle:
         lib.oracle_topk_ragged.restype = ctypes.c_int
         lib.oracle_topk_ragged.argtypes = [f32p, i32p, i32p, ctypes.c_int32,
                                            ctypes.c_int32, i32p, ctypes.c_int]
+        lib.oracle_topk_window.restype = ctypes.c_int
+        lib.oracle_topk_window.argtypes = [f32p, ctypes.c_int64, i32p, i32p, ctypes.c_int32,
+                                           ctypes.c_int32, i32p, ctypes.c_int]
         self.lib = lib
         self.path = lib_path
 
@@ -140,6 +143,23 @@ class Oracle:
             raise ValueError(f"oracle_topk_ragged: invalid arguments (status {rc})")
         return out
 
+    def topk_window(self, scores, starts, seq_lens, k: int, threads: int = 0) -> np.ndarray:
+        """scores [B, row_stride] fp32; row b selects among columns [starts[b],
+        seq_lens[b]) (clamped to the row) and emits those columns."""
+        s, sp = _f32(scores)
+        if s.ndim != 2:
+            raise ValueError("scores must be [batch, row_stride]")
+        st, stp = _i32(starts)
+        L, lp = _i32(seq_lens)
+        if st.shape != (s.shape[0],) or L.shape != (s.shape[0],):
+            raise ValueError("starts and seq_lens must both be [batch]")
+        out = np.empty((s.shape[0], k), dtype=np.int32)
+        _, op = _i32(out)
+        rc = self.lib.oracle_topk_window(sp, s.shape[1], stp, lp, s.shape[0], k, op, threads)
+        if rc != 0:
+            raise ValueError(f"oracle_topk_window: invalid arguments (status {rc})")
+        return out
+
     def run(self, w, threads: int = 0) -> np.ndarray:
         """Run one ``workloads.Workload``."""
         if w.form == "raw":
@@ -148,6 +168,8 @@ class Oracle:
             return self.topk_paged(w.scores, w.seq_lens, w.page_table, w.page_size, w.k, threads)
         if w.form == "ragged":
             return self.topk_ragged(w.scores, w.row_starts, w.seq_lens, w.k, threads)
+        if w.form == "window":
+            return self.topk_window(w.scores, w.row_starts, w.seq_lens, w.k, threads)
         raise ValueError(f"unknown form {w.form!r}")
 
 
@@ -178,6 +200,10 @@ def topk_paged(scores, seq_lens, page_table, page_size: int, k: int, threads: in
 
 def topk_ragged(scores, row_starts, seq_lens, k: int, threads: int = 0) -> np.ndarray:
     return default().topk_ragged(scores, row_starts, seq_lens, k, threads)
+
+
+def topk_window(scores, starts, seq_lens, k: int, threads: int = 0) -> np.ndarray:
+    return default().topk_window(scores, starts, seq_lens, k, threads)
 
 
 def run(w, threads: int = 0) -> np.ndarray:

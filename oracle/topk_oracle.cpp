@@ -34,6 +34,13 @@
 //        ragged: row_starts[b] + j   (the position inside the packed buffer;
 //                [37591] "关键源码片段", CoopParams, names row_starts as the
 //                row offsets of the ragged API but not the emitted value)
+//        window: lo + j, the column of the selected element in its row
+//   The window form ([37591] "实现拆解" item 3: the tests cover variable
+//   windows) selects among one window [lo, hi) of each row of a strided matrix:
+//   lo = starts[b] and hi = seq_lens[b], both clamped to [0, row_stride], and
+//   L = max(hi - lo, 0). With lo = 0 it is the raw form. (The pages name
+//   variable windows without defining them; a per-row [start, end) inside the
+//   row, emitting row columns, is the reading adopted.)
 //   5. Slots m .. k-1 get -1 ([36004] "关键源码片段": the test pre-fills the
 //      output with -1, so short rows leave -1 behind).
 //
@@ -74,13 +81,13 @@ void select_row(const float* row, int64_t L, int64_t k, std::vector<int32_t>& ch
   for (int64_t i = 0; i < m; ++i) chosen[i] = pairs[i].pos;
 }
 
-enum Form { kRaw = 0, kPaged = 1, kRagged = 2 };
+enum Form { kRaw = 0, kPaged = 1, kRagged = 2, kWindow = 3 };
 
 struct Job {
   Form form;
   const float* scores;
   int64_t row_stride;          // raw, paged
-  const int32_t* row_starts;   // ragged
+  const int32_t* row_starts;   // ragged: row offsets; window: window starts
   const int32_t* seq_lens;
   const int32_t* page_table;   // paged
   int64_t page_table_stride;   // paged
@@ -93,9 +100,15 @@ void run_row(const Job& job, int64_t b, std::vector<int32_t>& chosen) {
   const int64_t s = job.seq_lens[b];
   int64_t L;
   const float* row;
+  int64_t lo = 0;  // window: first column of the window
   if (job.form == kRagged) {
     L = std::max<int64_t>(s, 0);
     row = job.scores + job.row_starts[b];
+  } else if (job.form == kWindow) {
+    lo = std::clamp<int64_t>(job.row_starts[b], 0, job.row_stride);
+    const int64_t hi = std::clamp<int64_t>(s, 0, job.row_stride);
+    L = hi > lo ? hi - lo : 0;
+    row = job.scores + b * job.row_stride + lo;
   } else {
     L = std::min<int64_t>(std::max<int64_t>(s, 0), job.row_stride);
     row = job.scores + b * job.row_stride;
@@ -111,6 +124,8 @@ void run_row(const Job& job, int64_t b, std::vector<int32_t>& chosen) {
       v = pt[j / job.page_size] * job.page_size + j % job.page_size;
     } else if (job.form == kRagged) {
       v = job.row_starts[b] + j;
+    } else if (job.form == kWindow) {
+      v = static_cast<int32_t>(lo + j);
     }
     out[i] = v;
   }
@@ -135,7 +150,7 @@ int run(const Job& job, int32_t batch, int threads) {
     return 1;
   if (job.form != kRagged && job.row_stride < 1) return 1;
   if (job.form == kPaged && (job.page_table == nullptr || job.page_size < 1)) return 1;
-  if (job.form == kRagged && job.row_starts == nullptr) return 1;
+  if ((job.form == kRagged || job.form == kWindow) && job.row_starts == nullptr) return 1;
   if (batch == 0) return 0;
   if (threads < 1) threads = usable_cores();
   threads = std::min<int>(threads, batch);
@@ -189,6 +204,15 @@ int oracle_topk_ragged(const float* scores, const int32_t* row_starts,
                        const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
                        int threads) {
   Job job{kRagged, scores, 0, row_starts, seq_lens, nullptr, 0, 0, k, out};
+  return run(job, batch, threads);
+}
+
+// The window form: row b selects among scores[b, lo .. hi) with lo = starts[b]
+// and hi = seq_lens[b] (both clamped to [0, row_stride]) and emits columns lo + j.
+int oracle_topk_window(const float* scores, int64_t row_stride, const int32_t* starts,
+                       const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
+                       int threads) {
+  Job job{kWindow, scores, row_stride, starts, seq_lens, nullptr, 0, 0, k, out};
   return run(job, batch, threads);
 }
 

@@ -101,10 +101,17 @@ def check_workload(w, out: np.ndarray, max_rows: int | None = None) -> list[str]
     errors = []
     rows = range(w.batch) if max_rows is None else range(min(w.batch, max_rows))
     for b in rows:
-        if w.form == "ragged":
-            L = max(int(w.seq_lens[b]), 0)
-            start = int(w.row_starts[b])
-            row = w.scores[start:start + L]
+        if w.form in ("ragged", "window"):
+            if w.form == "ragged":
+                L = max(int(w.seq_lens[b]), 0)
+                start = int(w.row_starts[b])
+                row = w.scores[start:start + L]
+            else:  # columns [start, end) of row b, both clamped to the row
+                stride = w.scores.shape[1]
+                start = min(max(int(w.row_starts[b]), 0), stride)
+                end = min(max(int(w.seq_lens[b]), 0), stride)
+                L = max(end - start, 0)
+                row = w.scores[b, start:start + L]
             sel = np.where(out[b] >= 0, out[b].astype(np.int64) - start, out[b])
             sel = np.where((out[b] >= 0) & (sel < 0), -2, sel)
         else:

@@ -13,7 +13,9 @@ the first disagreement. The pins are:
   generator, with and without exact duplicates;
 * torch.topk (CPU) on continuous data without duplicate values;
 * cross-form identities: identity page table == raw, un-mapped permuted table
-  == raw, ragged row minus its start == raw of that row.
+  == raw, ragged row minus its start == raw of that row, window starting at 0 ==
+  raw, window minus its start == raw of the window's columns;
+* brute force over tiny windows (every k-subset of the window's columns).
 
 Run as a script (``python tests/oracle_pins.py <liboracle.so>``) it runs every pin
 but the torch one on the given library and exits 0 only if all pass; the
@@ -45,6 +47,8 @@ def run_case(o, c):
         return o.topk_raw(c.scores, c.seq_lens, c.k, 1)
     if c.form == "paged":
         return o.topk_paged(c.scores, c.seq_lens, c.page_table, c.page_size, c.k, 1)
+    if c.form == "window":
+        return o.topk_window(c.scores, c.row_starts, c.seq_lens, c.k, 1)
     return o.topk_ragged(c.scores, c.row_starts, c.seq_lens, c.k, 1)
 
 
@@ -103,6 +107,27 @@ def pin_brute_force(o, trials: int = 1500, seed: int = 7):
         got = set(int(v) for v in out if v >= 0)
         assert got == exp and int((out == -1).sum()) == k - len(exp), (
             f"trial {t}: row {row.tolist()} k={k}: oracle {out.tolist()}, brute force {sorted(exp)}")
+
+
+def pin_brute_force_window(o, trials: int = 600, seed: int = 29):
+    """Windows [start, end) of tiny rows, including ends outside the row and empty
+    windows, against enumeration over the window's columns."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    for t in range(trials):
+        stride = int(g.integers(1, 10))
+        row = tiny_row(g, stride)
+        start = int(g.integers(-2, stride + 2))
+        end = int(g.integers(-1, stride + 3))
+        k = int(g.integers(1, stride + 3))
+        out = o.topk_window(row[None, :], np.array([start], np.int32), np.array([end], np.int32),
+                            k, 1)[0]
+        lo, hi = min(max(start, 0), stride), min(max(end, 0), stride)
+        cols = list(range(lo, hi)) if hi > lo else []
+        exp = {cols[i] for i in brute_force([row[c] for c in cols], k)} if cols else set()
+        got = set(int(v) for v in out if v >= 0)
+        assert got == exp and int((out == -1).sum()) == k - len(exp), (
+            f"trial {t}: row {row.tolist()} [{start}, {end}) k={k}: oracle {out.tolist()}, "
+            f"brute force {sorted(exp)}")
 
 
 def pin_closed_form(o, seed: int = 11):
@@ -175,6 +200,20 @@ def pin_forms(o, seed: int = 19):
         assert (un == raw[b]).all(), f"ragged row {b} != raw"
     w = workloads.Workload("forms", "ragged", k, packed, lens.astype(np.int32), None, ps, starts)
     assert not check_workload(w, rag)
+    # window: starting at column 0 it is the raw form; otherwise, minus its start,
+    # it is the raw form of the window's columns
+    zero = np.zeros(B, np.int32)
+    assert (o.topk_window(scores, zero, seq, k, 1) == raw).all(), "window from 0 != raw"
+    wst = np.array([7, 1500, 0, 24], np.int32)
+    wen = np.array([2900, 2000, 499, 3100], np.int32)
+    win = o.topk_window(scores, wst, wen, k, 1)
+    for b in range(B):
+        hi = min(int(wen[b]), stride)
+        part = o.topk_raw(scores[b:b + 1, wst[b]:hi], np.array([hi - wst[b]], np.int32), k, 1)[0]
+        shifted = np.where(part >= 0, part + wst[b], -1)
+        assert (win[b] == shifted).all(), f"window row {b} != raw of its columns"
+    ww = workloads.Workload("forms", "window", k, scores, wen, None, ps, wst)
+    assert not check_workload(ww, win)
 
 
 def pin_threads(o, seed: int = 23):
@@ -184,7 +223,8 @@ def pin_threads(o, seed: int = 23):
     assert (o.topk_raw(scores, seq, 1024, 1) == o.topk_raw(scores, seq, 1024, 4)).all()
 
 
-CPU_PINS = (pin_golden, pin_brute_force, pin_closed_form, pin_invariants, pin_forms, pin_threads)
+CPU_PINS = (pin_golden, pin_brute_force, pin_brute_force_window, pin_closed_form, pin_invariants,
+            pin_forms, pin_threads)
 
 
 def main(argv):

@@ -36,6 +36,12 @@ MUTANTS = [
      "L = std::max<int64_t>(s, 0);"),
     ("row_stride_ignored", "row = job.scores + b * job.row_stride;",
      "row = job.scores + b * job.k;"),
+    ("window_offset_dropped", "v = static_cast<int32_t>(lo + j);", "v = j;"),
+    ("window_length_is_end", "L = hi > lo ? hi - lo : 0;", "L = hi;"),
+    ("window_start_below_zero_kept", "lo = std::clamp<int64_t>(job.row_starts[b], 0, job.row_stride);",
+     "lo = std::min<int64_t>(job.row_starts[b], job.row_stride);"),
+    ("window_row_not_offset", "row = job.scores + b * job.row_stride + lo;",
+     "row = job.scores + b * job.row_stride;"),
 ]
 
 

@@ -129,7 +129,10 @@ def pages_for(row_cap: int, page_size: int) -> int:
 
 @dataclasses.dataclass
 class Workload:
-    """One batch of inputs. ``form`` is "raw", "paged" or "ragged"."""
+    """One batch of inputs. ``form`` is "raw", "paged", "ragged" or "window".
+
+    window: row b of ``scores`` [B, row_stride] selects among its columns
+    [row_starts[b], seq_lens[b]) (both clamped to the row)."""
     name: str
     form: str
     k: int
@@ -137,7 +140,7 @@ class Workload:
     seq_lens: np.ndarray               # [B] int32
     page_table: np.ndarray | None = None   # [B, pages] int32 (paged)
     page_size: int = 64
-    row_starts: np.ndarray | None = None   # [B] int32 (ragged)
+    row_starts: np.ndarray | None = None   # [B] int32 (ragged: row offsets; window: starts)
 
     @property
     def batch(self) -> int:
@@ -149,6 +152,10 @@ class Workload:
         if self.form == "ragged":
             return int(np.maximum(self.seq_lens, 0).sum())
         cap = self.scores.shape[1]
+        if self.form == "window":
+            lo = np.clip(self.row_starts.astype(np.int64), 0, cap)
+            hi = np.clip(self.seq_lens.astype(np.int64), 0, cap)
+            return int(np.maximum(hi - lo, 0).sum())
         return int(np.clip(self.seq_lens, 0, cap).sum())
 
     def as_raw(self) -> "Workload":
@@ -215,6 +222,21 @@ def config5(batch: int, c4_len: int = 262144, seed: int = BASE_SEED + 4) -> Work
     seq = np.full(batch, c4_len, dtype=np.int32)
     pt = permuted_page_table(g, batch, pages_for(c4_len, 64))
     return Workload(f"paged_b{batch}_n{c4_len}_k2048_heavytail", "paged", 2048, scores, seq, pt, 64)
+
+
+def prefill_windows(batch: int, row_stride: int, window: int | None = None, k: int = 1024,
+                    seed: int = BASE_SEED + 5) -> Workload:
+    """Prefill-shaped rows: query b of the last ``batch`` tokens of a context of
+    ``row_stride`` keys attends causally to keys [start_b, end_b), end_b =
+    row_stride - batch + b + 1, start_b = max(0, end_b - window) (0 without a
+    sliding window). Scores: N(0,1) plus a per-row N(0, sigma=4) offset."""
+    g = rng(seed + batch + row_stride + (window or 0))
+    scores = decode(g, batch, row_stride)
+    ends = (row_stride - batch + np.arange(batch) + 1).clip(min=0).astype(np.int32)
+    starts = (np.zeros(batch, np.int32) if window is None
+              else np.maximum(ends - window, 0).astype(np.int32))
+    name = f"window_b{batch}_n{row_stride}_k{k}" + (f"_w{window}" if window else "_causal")
+    return Workload(name, "window", k, scores, ends, None, 64, starts)
 
 
 def random_rows(g: np.random.Generator, batch: int, row_stride: int, dist: str,
