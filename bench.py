@@ -73,6 +73,18 @@ def algorithmic_bytes(batch: int, L: int, k: int, form: str, page_size: int = PA
     return batch * per_row
 
 
+def workload_bytes(w, page_size: int = PAGE_SIZE) -> int:
+    """algorithmic_bytes for any workload: per row 4 L_b + 4 + 4 k, plus the page-table
+    entries (paged) or the row start / window start (ragged, window)."""
+    total = 4 * w.scored_elements + w.batch * (4 + 4 * w.k)
+    if w.form == "paged":
+        L = np.clip(w.seq_lens.astype(np.int64), 0, w.scores.shape[1])
+        total += int((4 * np.minimum(w.k, (L + page_size - 1) // page_size)).sum())
+    elif w.form in ("ragged", "window"):
+        total += 4 * w.batch
+    return int(total)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -196,6 +208,8 @@ def device_sets(w, n_sets, dev, torch):
              "out": torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)}
         if w.form == "paged":
             d["pt"] = torch.from_numpy(w.page_table).to(dev)
+        if w.form == "window":
+            d["starts"] = torch.from_numpy(w.row_starts).to(dev)
         sets.append(d)
     return sets
 
@@ -204,6 +218,9 @@ def call(pkg, w, d, stream):
     if w.form == "paged":
         pkg.topk_transform_paged(d["scores"], d["seq"], d["pt"], w.page_size, w.k, out=d["out"],
                                  stream=stream)
+    elif w.form == "window":
+        pkg.topk_transform_window(d["scores"], d["starts"], d["seq"], w.k, out=d["out"],
+                                  stream=stream)
     else:
         pkg.topk_transform_raw(d["scores"], d["seq"], w.k, out=d["out"], stream=stream)
 
@@ -396,6 +413,18 @@ def run_ours(args):
             ab = algorithmic_bytes(b, C4_LEN, ws.k, form)
             sweep.append({"batch": b, "form": form, "us_per_call": pc * 1e6,
                           "rows_per_s": b / pc, "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
+                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+        # prefill-shaped window rows: 4096 queries over a 32768-key context, causal and
+        # with a sliding window of 8192 keys
+        for window in (None, 8192):
+            ws = workloads.prefill_windows(4096, C4_LEN, window=window)
+            steps = 1000
+            s, _, _, ns = time_steps(pkg, ws, steps, 5, dev, torch, l2)
+            pc = s / steps
+            ab = workload_bytes(ws)
+            sweep.append({"batch": ws.batch, "form": "window", "workload": ws.name,
+                          "us_per_call": pc * 1e6, "rows_per_s": ws.batch / pc,
+                          "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
                           "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
         result["sweep"] = sweep
     if rank == 0:

@@ -5,6 +5,8 @@
  * What the operation computes (per row b of a batch):
  *   L = clamp(seq_lens[b], 0, row_stride)   (raw, paged)
  *     = max(seq_lens[b], 0)                 (ragged)
+ *     = max(hi - lo, 0)                     (window: lo = clamp(starts[b], 0, row_stride),
+ *                                            hi = clamp(seq_lens[b], 0, row_stride))
  *   Select the m = min(k, L) positions j < L whose fp32 scores are largest,
  *   exactly: scores are ranked by the order-preserving 32-bit key of their bit
  *   pattern (negative values bit-inverted, the others with the sign bit set),
@@ -17,11 +19,15 @@
  *     raw     j
  *     paged   page_table[b * page_table_stride + j / page_size] * page_size + j % page_size
  *     ragged  row_starts[b] + j
+ *     window  lo + j (the column in row b; position j of the window is column lo + j)
  *   and the slots m .. k-1 of the row are written with -1 (sglang PR #36004
  *   summary page, section "关键源码片段": test_deepseek_v4_topk_transform
  *   pre-fills the output with -1 and uses an identity page table, under which the
- *   paged slot equals the token position). The three entry points mirror the
- *   three API forms named on the PR #37591 page, "实现拆解" item 2.
+ *   paged slot equals the token position). The first three entry points mirror
+ *   the three API forms named on the PR #37591 page, "实现拆解" item 2. The window
+ *   form is the "variable windows" its tests cover (same page, item 3), read as
+ *   one [start, end) window per row of a strided matrix (prefill-shaped batches:
+ *   query b attends to keys start .. end-1).
  *
  * Output order: the order of the m positions inside out[b, 0:k) is unspecified;
  * compare rows as sets. The SET is deterministic.
@@ -37,17 +43,20 @@
  * Layouts (all row-major, int32 unless stated):
  *   scores      fp32, 4-byte aligned. raw/paged: row b starts at
  *               scores + b * row_stride (elements); ragged: row b starts at
- *               scores + row_starts[b]. Any alignment of a row start is accepted.
+ *               scores + row_starts[b]; window: row b's window starts at
+ *               scores + b * row_stride + lo. Any alignment of a row start is
+ *               accepted.
  *   seq_lens    [batch]
  *   page_table  [batch, page_table_stride]; entries are trusted: the entries for
  *               pages 0 .. ceil(L/page_size)-1 of each row must exist.
  *   row_starts  [batch], element offsets into `scores`; row_starts[b] + j must
  *               fit in int32.
+ *   starts      [batch] (window form), any int32 value: it is clamped as above.
  *   out         [batch, k]
  *
  * Errors: host-checkable problems return a status and launch nothing. Values
- * that live in device memory (seq_lens, page_table, row_starts) are not
- * validated: seq_lens are clamped as above, the others are trusted. A launch
+ * that live in device memory (seq_lens, page_table, row_starts, starts) are not
+ * validated: seq_lens and starts are clamped as above, the others are trusted. A launch
  * failure returns TOPK_ERR_CUDA; topk_last_cuda_error() gives the cudaError_t.
  */
 #ifndef TOPK_TRANSFORM_H_
@@ -104,6 +113,14 @@ int topk_transform_ragged(const float* scores, const int32_t* row_starts,
                           const int32_t* seq_lens, int64_t max_row_len_hint, int32_t batch,
                           int32_t k, int32_t* out, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
+
+/* Window form: row b of scores [batch, row_stride] selects among its columns
+ * [starts[b], seq_lens[b]) (both clamped to [0, row_stride]; an empty window if
+ * the end is not after the start) and writes the selected columns. With every
+ * start 0 it is the raw form. row_stride >= 1; starts, seq_lens [batch]. */
+int topk_transform_window(const float* scores, int64_t row_stride, const int32_t* starts,
+                          const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* A static English description of a status code. */
 const char* topk_status_string(int status);

@@ -25,7 +25,7 @@ from . import build as _build
 
 __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
-    "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged",
+    "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged", "topk_transform_window",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
@@ -67,6 +67,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_transform_paged.argtypes = [vp, i64, vp, vp, i64, i32, i32, i32, vp, vp, sz, vp]
             lib.topk_transform_ragged.restype = ctypes.c_int
             lib.topk_transform_ragged.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, sz, vp]
+            lib.topk_transform_window.restype = ctypes.c_int
+            lib.topk_transform_window.argtypes = [vp, i64, vp, vp, i32, i32, vp, vp, sz, vp]
             lib.topk_status_string.restype = ctypes.c_char_p
             lib.topk_status_string.argtypes = [ctypes.c_int]
             lib.topk_last_cuda_error.restype = ctypes.c_int
@@ -193,6 +195,24 @@ def topk_transform_ragged(scores: torch.Tensor, row_starts: torch.Tensor, seq_le
                                        seq_lens.data_ptr(), int(max_row_len_hint), batch, k,
                                        out.data_ptr(), None, 0, _stream(stream, dev))
     _check(st, "topk_transform_ragged")
+    return out
+
+
+def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: torch.Tensor,
+                          k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact top-k of each row's window of columns [starts[b], seq_lens[b]) (both
+    clamped to the row); the selected columns are written."""
+    lib = load_library()
+    batch, row_stride = _scores_2d(scores)
+    dev = scores.device
+    _vector(starts, "starts", batch, dev)
+    _vector(seq_lens, "seq_lens", batch, dev)
+    out = _out(out, batch, k, dev)
+    with torch.cuda.device(dev):
+        st = lib.topk_transform_window(scores.data_ptr(), row_stride, starts.data_ptr(),
+                                       seq_lens.data_ptr(), batch, k, out.data_ptr(), None, 0,
+                                       _stream(stream, dev))
+    _check(st, "topk_transform_window")
     return out
 
 

@@ -165,6 +165,18 @@ int topk_transform_ragged(const float* scores, const int32_t* row_starts,
   return run(topk_gb300::kRagged, p, max_row_len_hint, stream);
 }
 
+int topk_transform_window(const float* scores, int64_t row_stride, const int32_t* starts,
+                          const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
+                          void* /*workspace*/, size_t /*workspace_bytes*/, cudaStream_t stream) {
+  const int st = check_common(scores, seq_lens, batch, k, out);
+  if (st != TOPK_OK || batch == 0) return st;
+  if (row_stride < 1 || starts == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  Params p = base_params(scores, seq_lens, batch, k, out);
+  p.row_stride = row_stride;
+  p.row_starts = starts;
+  return run(topk_gb300::kWindow, p, row_stride, stream);
+}
+
 const char* topk_status_string(int status) {
   switch (status) {
     case TOPK_OK: return "ok";

@@ -512,7 +512,7 @@ struct OutMap {
   const int32_t* pt_smem; // paged: the same entries staged in shared memory, or null
   int32_t ps;             // page size
   int32_t ps_shift;       // log2(ps) or -1
-  int32_t rstart;         // ragged: row start in the packed buffer
+  int32_t rstart;         // ragged: row start in the packed buffer; window: its first column
 };
 
 template <int F>
@@ -528,7 +528,7 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
     }
     const int32_t phys = m.pt_smem != nullptr ? m.pt_smem[page] : __ldg(m.pt_row + page);
     return phys * m.ps + off;
-  } else if constexpr (F == kRagged) {
+  } else if constexpr (F == kRagged || F == kWindow) {
     return m.rstart + j;
   } else {
     return j;
@@ -1206,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // later) while the length is still on its way
   Sample sm;
   bool sample_loaded = false;
-  if constexpr (F != kRagged) {
+  if constexpr (F == kRaw || F == kPaged) {
     if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
       load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
                              static_cast<int32_t>(p.row_stride), rank, G),
@@ -1218,6 +1218,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     m.rstart = p.row_starts[row];
     rowp = p.scores + m.rstart;
     L = max(seq, 0);
+  } else if constexpr (F == kWindow) {  // columns [lo, hi) of the row, clamped to it
+    const int64_t hi = min(static_cast<int64_t>(max(seq, 0)), p.row_stride);
+    const int64_t lo = min(static_cast<int64_t>(max(p.row_starts[row], 0)), hi);
+    m.rstart = static_cast<int32_t>(lo);
+    rowp = p.scores + static_cast<int64_t>(row) * p.row_stride + lo;
+    L = static_cast<int32_t>(hi - lo);
   } else {
     rowp = p.scores + static_cast<int64_t>(row) * p.row_stride;
     L = static_cast<int32_t>(min(static_cast<int64_t>(max(seq, 0)), p.row_stride));
@@ -1428,6 +1434,7 @@ cudaError_t prepare_device() {
   cudaError_t e = prepare_form<kRaw>();
   if (e == cudaSuccess) e = prepare_form<kPaged>();
   if (e == cudaSuccess) e = prepare_form<kRagged>();
+  if (e == cudaSuccess) e = prepare_form<kWindow>();
   return e;
 }
 
@@ -1436,6 +1443,7 @@ cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream) {
     case kRaw: return launch_form<kRaw>(p, g, stream);
     case kPaged: return launch_form<kPaged>(p, g, stream);
     case kRagged: return launch_form<kRagged>(p, g, stream);
+    case kWindow: return launch_form<kWindow>(p, g, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -8,7 +8,7 @@
 
 namespace topk_gb300 {
 
-enum Form : int { kRaw = 0, kPaged = 1, kRagged = 2 };
+enum Form : int { kRaw = 0, kPaged = 1, kRagged = 2, kWindow = 3 };
 
 constexpr int kThreads = 512;          // threads per CTA
 constexpr int kMaxBins = 4096;         // widest histogram (12 key bits)
@@ -17,9 +17,9 @@ constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster siz
 
 struct Params {
   const float* scores;
-  int64_t row_stride;          // raw, paged: elements between row starts
+  int64_t row_stride;          // raw, paged, window: elements between row starts
   const int32_t* seq_lens;     // [batch]
-  const int32_t* row_starts;   // ragged: [batch]
+  const int32_t* row_starts;   // ragged: row offsets [batch]; window: window starts [batch]
   const int32_t* page_table;   // paged: [batch, pt_stride]
   int64_t pt_stride;
   int32_t page_size;

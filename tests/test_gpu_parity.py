@@ -56,6 +56,9 @@ def run_gpu(pkg, w, stream=None) -> np.ndarray:
     elif w.form == "paged":
         pt = torch.from_numpy(np.ascontiguousarray(w.page_table)).to(dev)
         pkg.topk_transform_paged(scores, seq, pt, w.page_size, w.k, out=out, stream=stream)
+    elif w.form == "window":
+        st = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
+        pkg.topk_transform_window(scores, st, seq, w.k, out=out, stream=stream)
     else:
         rs = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
         hint = int(np.max(w.seq_lens, initial=0))
@@ -305,3 +308,76 @@ def test_candidate_counts_off_block_multiples(pkg, split):
     with settings(pkg, split=split):
         got = run_gpu(pkg, w)
     assert_parity(w, got)
+
+
+# ------------------------------------------------------------ window form (prefill-shaped rows)
+
+def window_rows(w, rows):
+    """The sub-batch of a window workload made of the given rows."""
+    import dataclasses
+    return dataclasses.replace(w, name=f"{w.name}_rows", scores=w.scores[rows],
+                               seq_lens=w.seq_lens[rows], row_starts=w.row_starts[rows])
+
+
+@pytest.mark.parametrize("window", [None, 3000, 1000])
+def test_window_prefill(pkg, window):
+    w = workloads.prefill_windows(512, 8192, window=window)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+def test_window_prefill_bench_size(pkg):
+    """4096 causal rows of a 32768-key context, the launch bench.py times; 256
+    sampled rows against the oracle, every row through the invariant check."""
+    w = workloads.prefill_windows(4096, 32768)
+    got = run_gpu(pkg, w)
+    rows = np.random.Generator(np.random.PCG64(3)).choice(w.batch, 256, replace=False)
+    rows = np.sort(np.concatenate([rows, [0, w.batch - 1]]))
+    sub = window_rows(w, rows)
+    assert same_sets(got[rows], oracle.run(sub)).all()
+    assert not check_workload(w, got, max_rows=None if w.batch <= 512 else 512)
+
+
+def random_windows(seed, batch, stride, dist, k):
+    g = np.random.Generator(np.random.PCG64(seed))
+    scores = workloads.random_rows(g, batch, stride, dist, dup=True)
+    starts = g.integers(-5, stride + 5, size=batch)
+    ends = g.integers(-5, stride + 6, size=batch)
+    # a share of long windows, so the sampled filter runs, and a few exact edges
+    long_rows = g.random(batch) < 0.5
+    starts[long_rows] = g.integers(-3, 9, size=int(long_rows.sum()))
+    ends[long_rows] = g.integers(stride - 9, stride + 4, size=int(long_rows.sum()))
+    starts[:4] = [0, stride, 3, stride - k]
+    ends[:4] = [stride, stride, 2, stride]
+    return workloads.Workload(f"window_random_{dist}_{stride}", "window", k, scores,
+                              ends.astype(np.int32), None, 64, starts.astype(np.int32))
+
+
+@pytest.mark.parametrize("split", [1, 4, 16])
+@pytest.mark.parametrize("fast", [1, 0])
+@pytest.mark.parametrize("dist", ["normal", "banded", "narrow"])
+def test_window_random(pkg, split, fast, dist):
+    w = random_windows(101 + split + 7 * fast, 48, 9001, dist, 1024)
+    with settings(pkg, split=split, fast=fast):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("tie_cap", [0, 64, 1500])
+def test_window_small_tie_buffer(pkg, tie_cap):
+    w = random_windows(211 + tie_cap, 24, 6007, "banded", 512)
+    with settings(pkg, tie_cap=tie_cap):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("k", [1, 5, 2048])
+def test_window_any_k(pkg, k):
+    w = random_windows(307 + k, 16, 5003, "heavy_tail", k)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+def test_window_from_zero_is_raw(pkg):
+    w = workloads.config3(8, "raw", c4_len=9000)
+    ww = workloads.Workload("window_zero", "window", w.k, w.scores, w.seq_lens, None, 64,
+                            np.zeros(w.batch, np.int32))
+    assert same_sets(run_gpu(pkg, ww), run_gpu(pkg, w)).all()
