@@ -265,6 +265,58 @@ def time_steps(pkg, w, steps, warmup, dev, torch, l2_bytes, dist=None, clocks=No
     return secs, steps, (t0, t1), n_sets
 
 
+def time_grouped(pkg, ws, steps, dev, torch, l2_bytes):
+    """The problems ws as one grouped call and as separate calls, each step on its
+    own rotating input set (CUDA graph replay); returns (grouped s, separate s)."""
+    set_bytes = sum(w.scores.nbytes + w.seq_lens.nbytes
+                    + (w.page_table.nbytes if w.form == "paged" else 0) for w in ws)
+    n_sets = max(2, min(1024, math.ceil(L2_FACTOR * l2_bytes / set_bytes)))
+    sets = [[device_sets(w, 1, dev, torch)[0] for w in ws] for _ in range(n_sets)]
+
+    def grouped(ds):
+        probs = []
+        for w, d in zip(ws, ds):
+            q = {"form": w.form, "k": w.k, "scores": d["scores"], "seq_lens": d["seq"],
+                 "out": d["out"]}
+            if w.form == "paged":
+                q["page_table"], q["page_size"] = d["pt"], w.page_size
+            probs.append(q)
+        return probs
+
+    probs = [grouped(ds) for ds in sets]
+    stream = torch.cuda.Stream(dev)
+    result = []
+    for mode in ("grouped", "separate"):
+        with torch.cuda.stream(stream):
+            def one(i):
+                if mode == "grouped":
+                    pkg.topk_transform_grouped(probs[i], stream=stream)
+                else:
+                    for w, d in zip(ws, sets[i]):
+                        call(pkg, w, d, stream)
+            for i in range(n_sets):
+                one(i)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(n_sets):
+                    one(i)
+            graph.replay()
+            stream.synchronize()
+            reps = max(1, steps // n_sets)
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            end.record(stream)
+            end.synchronize()
+            result.append(start.elapsed_time(end) / 1e3 / (reps * n_sets))
+            del graph
+    del sets, probs
+    torch.cuda.empty_cache()
+    return tuple(result)
+
+
 def time_e2e(pkg, w, steps, dev, torch):
     """Same call with pinned host inputs: H2D of scores/seq_lens/page_table, the
     kernel, D2H of the result, every step, inside the timed region."""
@@ -426,6 +478,14 @@ def run_ours(args):
                           "us_per_call": pc * 1e6, "rows_per_s": ws.batch / pc,
                           "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
                           "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+        # several independent problems per step: four C3 paged batches of 64 rows, as
+        # one grouped call (one launch) and as four calls
+        ws4 = [workloads.config3(64, seed=workloads.BASE_SEED + 2 + 1000 * i) for i in range(4)]
+        tg, tsep = time_grouped(pkg, ws4, 2000, dev, torch, l2)
+        ab = sum(workload_bytes(w) for w in ws4)
+        sweep.append({"batch": 256, "form": "grouped", "workload": "4 x paged B=64 c4_len=32768 k=1024",
+                      "us_per_call": tg * 1e6, "us_per_call_separate": tsep * 1e6,
+                      "gbs": ab / tg / 1e9, "frac": ab / tg / 1e9 / peak})
         result["sweep"] = sweep
     if rank == 0:
         print(json.dumps(result), flush=True)

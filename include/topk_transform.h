@@ -122,6 +122,55 @@ int topk_transform_window(const float* scores, int64_t row_stride, const int32_t
                           const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------ grouped calls
+ *
+ * Several independent transforms in as few launches as possible: one launch per
+ * form present, in which the rows of every problem of that form run
+ * concurrently (the per-decode-step batching of the PR #37591 page's serving
+ * context: the many small top-k calls of one step no longer run one after the
+ * other). The result of each problem is exactly what the entry point of its form
+ * writes. */
+typedef enum {
+  TOPK_FORM_RAW = 0,
+  TOPK_FORM_PAGED = 1,
+  TOPK_FORM_RAGGED = 2,
+  TOPK_FORM_WINDOW = 3
+} topk_form_t;
+
+/* One problem: the arguments of its form's entry point. Fields a form does not
+ * use are ignored (row_stride: raw, paged, window; page_table, page_table_stride,
+ * page_size: paged; row_starts: ragged row offsets or window starts;
+ * max_row_len_hint: ragged). */
+typedef struct {
+  int32_t form;               /* topk_form_t */
+  int32_t batch;              /* rows, >= 0 (0: nothing to do) */
+  int32_t k;                  /* [1, TOPK_MAX_K] */
+  int32_t page_size;
+  int64_t row_stride;
+  int64_t page_table_stride;
+  int64_t max_row_len_hint;
+  const float* scores;
+  const int32_t* seq_lens;
+  const int32_t* row_starts;
+  const int32_t* page_table;
+  int32_t* out;               /* [batch, k] */
+} topk_problem_t;
+
+/* Most problems one grouped call takes. */
+#define TOPK_MAX_GROUP 32
+
+/* sizeof(topk_problem_t) as this library was built (for bindings to check their
+ * copy of the layout). */
+size_t topk_problem_bytes(void);
+
+/* problems: HOST array of n_problems (0 .. TOPK_MAX_GROUP) descriptors, read
+ * during the call only; the pointers inside are device memory, as for the single
+ * entry points. Every problem is checked first, in order: on the first problem
+ * that fails its check nothing is launched and its status is returned.
+ * Problems of one form share a launch; distinct output buffers are required. */
+int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* A static English description of a status code. */
 const char* topk_status_string(int status);
 

@@ -26,6 +26,7 @@ from . import build as _build
 __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
     "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged", "topk_transform_window",
+    "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
@@ -69,6 +70,13 @@ def load_library() -> ctypes.CDLL:
             lib.topk_transform_ragged.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, sz, vp]
             lib.topk_transform_window.restype = ctypes.c_int
             lib.topk_transform_window.argtypes = [vp, i64, vp, vp, i32, i32, vp, vp, sz, vp]
+            lib.topk_transform_grouped.restype = ctypes.c_int
+            lib.topk_transform_grouped.argtypes = [vp, i32, vp, sz, vp]
+            lib.topk_problem_bytes.restype = sz
+            lib.topk_problem_bytes.argtypes = []
+            if lib.topk_problem_bytes() != ctypes.sizeof(TopkProblem):
+                raise RuntimeError("topk_problem_t layout differs between the library and "
+                                   "this binding")
             lib.topk_status_string.restype = ctypes.c_char_p
             lib.topk_status_string.argtypes = [ctypes.c_int]
             lib.topk_last_cuda_error.restype = ctypes.c_int
@@ -214,6 +222,83 @@ def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: 
                                        _stream(stream, dev))
     _check(st, "topk_transform_window")
     return out
+
+
+TOPK_MAX_GROUP = 32
+_FORMS = {"raw": 0, "paged": 1, "ragged": 2, "window": 3}
+
+
+class TopkProblem(ctypes.Structure):
+    """ctypes copy of topk_problem_t (include/topk_transform.h)."""
+    _fields_ = [("form", ctypes.c_int32), ("batch", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("row_stride", ctypes.c_int64),
+                ("page_table_stride", ctypes.c_int64), ("max_row_len_hint", ctypes.c_int64),
+                ("scores", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("row_starts", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
+
+
+def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tensor]:
+    """Several independent transforms in one call (one launch per form present).
+
+    Each problem is a dict with "form" ("raw", "paged", "ragged" or "window"), "k",
+    "scores", "seq_lens" and what its form needs: "page_table" and "page_size"
+    (paged), "row_starts" and optionally "max_row_len_hint" (ragged), "starts"
+    (window); "out" is optional. Returns the output tensors, in order."""
+    lib = load_library()
+    if len(problems) > TOPK_MAX_GROUP:
+        raise ValueError(f"at most {TOPK_MAX_GROUP} problems per grouped call")
+    arr = (TopkProblem * max(len(problems), 1))()
+    outs, dev = [], None
+    for i, q in enumerate(problems):
+        form = q["form"]
+        if form not in _FORMS:
+            raise ValueError(f"unknown form {form!r}")
+        k = int(q["k"])
+        scores = q["scores"]
+        d = scores.device
+        if dev is None:
+            dev = d
+        elif d != dev:
+            raise ValueError("all problems of a grouped call must be on one device")
+        if form == "ragged":
+            _cuda_tensor(scores, "scores", torch.float32)
+            if scores.dim() != 1 or (scores.numel() > 1 and scores.stride(0) != 1):
+                raise ValueError("ragged scores must be a contiguous 1-D fp32 tensor")
+            batch = int(q["row_starts"].shape[0])
+            _vector(q["row_starts"], "row_starts", batch, d)
+            arr[i].row_starts = q["row_starts"].data_ptr()
+            arr[i].max_row_len_hint = int(q.get("max_row_len_hint", 0))
+        else:
+            batch, arr[i].row_stride = _scores_2d(scores)
+        _vector(q["seq_lens"], "seq_lens", batch, d)
+        if form == "paged":
+            pt = q["page_table"]
+            _cuda_tensor(pt, "page_table", torch.int32, d)
+            if pt.dim() != 2 or pt.shape[0] != batch or (pt.shape[1] > 1 and pt.stride(1) != 1):
+                raise ValueError("page_table must be [batch, pages] int32 with unit inner stride")
+            pt_stride = int(pt.stride(0)) if batch > 1 else int(pt.shape[1])
+            if pt_stride < max(int(pt.shape[1]), 1):
+                raise ValueError("page_table rows must not overlap (use .contiguous() on expanded tables)")
+            if pt.shape[1] * int(q["page_size"]) < scores.shape[1]:
+                raise ValueError("page_table has too few pages for the rows")
+            arr[i].page_table = pt.data_ptr()
+            arr[i].page_table_stride = pt_stride
+            arr[i].page_size = int(q["page_size"])
+        elif form == "window":
+            _vector(q["starts"], "starts", batch, d)
+            arr[i].row_starts = q["starts"].data_ptr()
+        out = _out(q.get("out"), batch, k, d)
+        arr[i].form, arr[i].batch, arr[i].k = _FORMS[form], batch, k
+        arr[i].scores, arr[i].seq_lens, arr[i].out = scores.data_ptr(), q["seq_lens"].data_ptr(), out.data_ptr()
+        outs.append(out)
+    if not problems:
+        return outs
+    with torch.cuda.device(dev):
+        st = lib.topk_transform_grouped(ctypes.addressof(arr), len(problems), None, 0,
+                                        _stream(stream, dev))
+    _check(st, "topk_transform_grouped")
+    return outs
 
 
 def topk_set_row_split(g: int) -> int:

@@ -48,7 +48,7 @@ int row_split_setting() {
 // 32 blocks, none when fewer than 4). Here a split costs no extra launch (the CTAs
 // of a cluster merge histograms in distributed shared memory); the rule below is
 // the measured one. row_len <= 0 means unknown: treated as long.
-int choose_split(int32_t batch, int64_t row_len, int sm_count) {
+int choose_split(int64_t batch, int64_t row_len, int sm_count) {
   const int forced = row_split_setting();
   if (forced >= 1) {
     int g = 1;
@@ -65,7 +65,7 @@ int choose_split(int32_t batch, int64_t row_len, int sm_count) {
   const int64_t slots = static_cast<int64_t>(sm_count) * 2;
   int g = 1;
   while (g < topk_gb300::kMaxCluster && len / (g * 2) >= 8192) g *= 2;
-  while (g > 1 && static_cast<int64_t>(batch) * g > slots) g /= 2;
+  while (g > 1 && batch * g > slots) g /= 2;
   return g >= 4 ? g : 1;
 }
 
@@ -74,7 +74,8 @@ int fail_cuda(cudaError_t e) {
   return TOPK_ERR_CUDA;
 }
 
-int run(Form form, Params p, int64_t row_len_hint, cudaStream_t stream) {
+// The current device's state, set up on first use (SM count, kernel attributes).
+int device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -85,36 +86,92 @@ int run(Form form, Params p, int64_t row_len_hint, cudaStream_t stream) {
     if (ds.err == cudaSuccess) ds.err = topk_gb300::prepare_device();
   });
   if (ds.err != cudaSuccess) return fail_cuda(ds.err);
-  const int g = choose_split(p.batch, row_len_hint, ds.sm_count);
+  *out = &ds;
+  return TOPK_OK;
+}
+
+// Checks one problem on the host and fills its kernel parameters; *len_hint gets
+// the longest row it can have (for the row split). Nothing in device memory is
+// read.
+int build_params(const topk_problem_t& q, Params* p, int64_t* len_hint) {
+  if (q.batch < 0) return TOPK_ERR_INVALID_ARGUMENT;
+  if (q.k < 1 || q.k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED_K;
+  if (q.form < TOPK_FORM_RAW || q.form > TOPK_FORM_WINDOW) return TOPK_ERR_INVALID_ARGUMENT;
+  *p = Params{};
+  p->batch = q.batch;
+  p->k = q.k;
+  p->page_size = 1;
+  p->page_shift = 0;
+  if (q.batch == 0) return TOPK_OK;
+  if (q.scores == nullptr || q.seq_lens == nullptr || q.out == nullptr)
+    return TOPK_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(q.scores) & 3u) != 0) return TOPK_ERR_INVALID_ARGUMENT;
+  p->scores = q.scores;
+  p->seq_lens = q.seq_lens;
+  p->out = q.out;
+  if (q.form == TOPK_FORM_RAGGED) {
+    if (q.row_starts == nullptr || q.max_row_len_hint < 0) return TOPK_ERR_INVALID_ARGUMENT;
+    p->row_starts = q.row_starts;
+    *len_hint = q.max_row_len_hint;
+    return TOPK_OK;
+  }
+  if (q.row_stride < 1) return TOPK_ERR_INVALID_ARGUMENT;
+  p->row_stride = q.row_stride;
+  *len_hint = q.row_stride;
+  if (q.form == TOPK_FORM_PAGED) {
+    if (q.page_table == nullptr || q.page_table_stride < 1 || q.page_size < 1)
+      return TOPK_ERR_INVALID_ARGUMENT;
+    p->page_table = q.page_table;
+    p->pt_stride = q.page_table_stride;
+    p->page_size = q.page_size;
+    p->page_shift = (q.page_size & (q.page_size - 1)) == 0 ? __builtin_ctz(q.page_size) : -1;
+  } else if (q.form == TOPK_FORM_WINDOW) {
+    if (q.row_starts == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+    p->row_starts = q.row_starts;
+  }
+  return TOPK_OK;
+}
+
+// The process-wide knobs, read once per call (every problem of a launch must see
+// the same tie capacity: it sizes the launch's shared memory).
+struct Settings {
+  int tie_cap, use_filter;
+};
+Settings settings() {
+  return Settings{g_tie_cap.load(std::memory_order_relaxed),
+                  g_fast_tier.load(std::memory_order_relaxed)};
+}
+void apply_settings(const Settings& s, Params* p) {
+  p->tie_cap = s.tie_cap;
+  p->use_filter = s.use_filter;
+}
+
+int run_one(const topk_problem_t& q, cudaStream_t stream) {
+  Params p;
+  int64_t hint = 0;
+  int st = build_params(q, &p, &hint);
+  if (st != TOPK_OK || q.batch == 0) return st;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != TOPK_OK) return st;
+  const int g = choose_split(p.batch, hint, ds->sm_count);
   if (static_cast<int64_t>(p.batch) * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
-  p.tie_cap = g_tie_cap.load(std::memory_order_relaxed);
-  p.use_filter = g_fast_tier.load(std::memory_order_relaxed);
-  e = topk_gb300::launch(form, p, g, stream);
-  if (e != cudaSuccess) return fail_cuda(e);
-  return TOPK_OK;
+  apply_settings(settings(), &p);
+  const cudaError_t e = topk_gb300::launch(static_cast<Form>(q.form), p, g, stream);
+  return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
 }
 
-int check_common(const float* scores, const int32_t* seq_lens, int32_t batch, int32_t k,
-                 const int32_t* out) {
-  if (batch < 0) return TOPK_ERR_INVALID_ARGUMENT;
-  if (k < 1 || k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED_K;
-  if (batch == 0) return TOPK_OK;
-  if (scores == nullptr || seq_lens == nullptr || out == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
-  if ((reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return TOPK_ERR_INVALID_ARGUMENT;
-  return TOPK_OK;
-}
-
-Params base_params(const float* scores, const int32_t* seq_lens, int32_t batch, int32_t k,
-                   int32_t* out) {
-  Params p = {};
-  p.scores = scores;
-  p.seq_lens = seq_lens;
-  p.batch = batch;
-  p.k = k;
-  p.out = out;
-  p.page_size = 1;
-  p.page_shift = 0;
-  return p;
+topk_problem_t problem(int32_t form, const float* scores, int64_t row_stride,
+                       const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out) {
+  topk_problem_t q = {};
+  q.form = form;
+  q.scores = scores;
+  q.row_stride = row_stride;
+  q.seq_lens = seq_lens;
+  q.batch = batch;
+  q.k = k;
+  q.out = out;
+  return q;
 }
 
 }  // namespace
@@ -125,56 +182,88 @@ size_t topk_workspace_bytes(int32_t /*batch*/, int64_t /*max_row_len*/, int32_t 
   return 0;
 }
 
+size_t topk_problem_bytes(void) { return sizeof(topk_problem_t); }
+
 int topk_transform_raw(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                        int32_t batch, int32_t k, int32_t* out, void* /*workspace*/,
                        size_t /*workspace_bytes*/, cudaStream_t stream) {
-  const int st = check_common(scores, seq_lens, batch, k, out);
-  if (st != TOPK_OK || batch == 0) return st;
-  if (row_stride < 1) return TOPK_ERR_INVALID_ARGUMENT;
-  Params p = base_params(scores, seq_lens, batch, k, out);
-  p.row_stride = row_stride;
-  return run(topk_gb300::kRaw, p, row_stride, stream);
+  return run_one(problem(TOPK_FORM_RAW, scores, row_stride, seq_lens, batch, k, out), stream);
 }
 
 int topk_transform_paged(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                          const int32_t* page_table, int64_t page_table_stride,
                          int32_t page_size, int32_t batch, int32_t k, int32_t* out,
                          void* /*workspace*/, size_t /*workspace_bytes*/, cudaStream_t stream) {
-  const int st = check_common(scores, seq_lens, batch, k, out);
-  if (st != TOPK_OK || batch == 0) return st;
-  if (row_stride < 1 || page_table == nullptr || page_table_stride < 1 || page_size < 1)
-    return TOPK_ERR_INVALID_ARGUMENT;
-  Params p = base_params(scores, seq_lens, batch, k, out);
-  p.row_stride = row_stride;
-  p.page_table = page_table;
-  p.pt_stride = page_table_stride;
-  p.page_size = page_size;
-  p.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz(page_size) : -1;
-  return run(topk_gb300::kPaged, p, row_stride, stream);
+  topk_problem_t q = problem(TOPK_FORM_PAGED, scores, row_stride, seq_lens, batch, k, out);
+  q.page_table = page_table;
+  q.page_table_stride = page_table_stride;
+  q.page_size = page_size;
+  return run_one(q, stream);
 }
 
 int topk_transform_ragged(const float* scores, const int32_t* row_starts,
                           const int32_t* seq_lens, int64_t max_row_len_hint, int32_t batch,
                           int32_t k, int32_t* out, void* /*workspace*/,
                           size_t /*workspace_bytes*/, cudaStream_t stream) {
-  const int st = check_common(scores, seq_lens, batch, k, out);
-  if (st != TOPK_OK || batch == 0) return st;
-  if (row_starts == nullptr || max_row_len_hint < 0) return TOPK_ERR_INVALID_ARGUMENT;
-  Params p = base_params(scores, seq_lens, batch, k, out);
-  p.row_starts = row_starts;
-  return run(topk_gb300::kRagged, p, max_row_len_hint, stream);
+  topk_problem_t q = problem(TOPK_FORM_RAGGED, scores, 0, seq_lens, batch, k, out);
+  q.row_starts = row_starts;
+  q.max_row_len_hint = max_row_len_hint;
+  return run_one(q, stream);
 }
 
 int topk_transform_window(const float* scores, int64_t row_stride, const int32_t* starts,
                           const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
                           void* /*workspace*/, size_t /*workspace_bytes*/, cudaStream_t stream) {
-  const int st = check_common(scores, seq_lens, batch, k, out);
-  if (st != TOPK_OK || batch == 0) return st;
-  if (row_stride < 1 || starts == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
-  Params p = base_params(scores, seq_lens, batch, k, out);
-  p.row_stride = row_stride;
-  p.row_starts = starts;
-  return run(topk_gb300::kWindow, p, row_stride, stream);
+  topk_problem_t q = problem(TOPK_FORM_WINDOW, scores, row_stride, seq_lens, batch, k, out);
+  q.row_starts = starts;
+  return run_one(q, stream);
+}
+
+int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
+                           void* /*workspace*/, size_t /*workspace_bytes*/,
+                           cudaStream_t stream) {
+  if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
+  if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  // every problem is checked before anything is launched
+  static_assert(TOPK_MAX_GROUP <= topk_gb300::kMaxGroup, "group limit");
+  Params params[TOPK_MAX_GROUP];
+  int64_t hints[TOPK_MAX_GROUP];
+  int64_t rows_of_form[4] = {0, 0, 0, 0};
+  for (int i = 0; i < n_problems; ++i) {
+    hints[i] = 0;
+    const int st = build_params(problems[i], &params[i], &hints[i]);
+    if (st != TOPK_OK) return st;
+    rows_of_form[problems[i].form] += problems[i].batch;
+  }
+  DeviceState* ds = nullptr;
+  bool any = false;
+  for (int f = 0; f < 4; ++f) any = any || rows_of_form[f] > 0;
+  if (!any) return TOPK_OK;
+  int st = device_state(&ds);
+  if (st != TOPK_OK) return st;
+  const Settings knobs = settings();
+  for (int f = 0; f < 4; ++f) {
+    if (rows_of_form[f] == 0) continue;
+    topk_gb300::GroupParams gp;
+    gp.n = 0;
+    int64_t rows = 0, hint = 0;
+    for (int i = 0; i < n_problems; ++i) {
+      if (problems[i].form != f || problems[i].batch == 0) continue;
+      apply_settings(knobs, &params[i]);
+      gp.probs[gp.n] = params[i];
+      gp.row_begin[gp.n] = static_cast<int32_t>(rows);
+      rows += problems[i].batch;
+      // the longest row decides the split; ragged rows of unknown length count as long
+      hint = (hint < 0 || hints[i] <= 0) ? -1 : (hints[i] > hint ? hints[i] : hint);
+      ++gp.n;
+    }
+    const int g = choose_split(rows, hint < 0 ? 0 : hint, ds->sm_count);
+    if (rows * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
+    gp.row_begin[gp.n] = static_cast<int32_t>(rows);
+    const cudaError_t e = topk_gb300::launch_group(static_cast<Form>(f), gp, g, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return TOPK_OK;
 }
 
 const char* topk_status_string(int status) {

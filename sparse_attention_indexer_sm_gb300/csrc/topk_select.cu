@@ -1158,14 +1158,11 @@ __device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t
 
 // ------------------------------------------------------------------ the kernel
 
+// One row of problem p, this CTA's slice of it (CTA `rank` of a cluster of G).
 template <int F>
-__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
-  extern __shared__ __align__(16) uint32_t dyn[];
-  __shared__ Ctl ctl;
+__device__ __forceinline__ void row_body(const Params& p, int row, int G, int rank, uint32_t* dyn,
+                                         Ctl& ctl) {
   const int tid = threadIdx.x;
-  const int G = static_cast<int>(cluster_nctarank());
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int row = static_cast<int>(blockIdx.x) / G;
 
   // shared memory: histogram | list | page table | cluster-sum histogram (G > 1) |
   // candidate/tie buffer
@@ -1396,12 +1393,41 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   }
 }
 
+// One cluster of G CTAs per row.
 template <int F>
-cudaError_t launch_form(const Params& p, int g, cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  __shared__ Ctl ctl;
+  const int G = static_cast<int>(cluster_nctarank());
+  row_body<F>(p, static_cast<int>(blockIdx.x) / G, G, static_cast<int>(cluster_ctarank()), dyn,
+              ctl);
+}
+
+// Several problems of one form in one launch: the clusters take the problems' rows
+// in order (problem i owns rows [row_begin[i], row_begin[i + 1])). Each CTA copies
+// its problem's parameters to shared memory once.
+template <int F>
+__global__ void __launch_bounds__(kThreads, 2)
+    topk_group_kernel(const __grid_constant__ GroupParams gp) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  __shared__ Ctl ctl;
+  __shared__ Params prob;
+  const int G = static_cast<int>(cluster_nctarank());
+  const int item = static_cast<int>(blockIdx.x) / G;
+  int i = 0;
+  while (i + 1 < gp.n && gp.row_begin[i + 1] <= item) ++i;
+  if (threadIdx.x == 0) prob = gp.probs[i];
+  __syncthreads();
+  row_body<F>(prob, item - gp.row_begin[i], G, static_cast<int>(cluster_ctarank()), dyn, ctl);
+}
+
+template <class Kernel, class Arg>
+cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, int tie_cap,
+                            cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * static_cast<unsigned>(g), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * g), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(g, p.tie_cap);
+  cfg.dynamicSmemBytes = smem_bytes(g, tie_cap);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1410,17 +1436,32 @@ cudaError_t launch_form(const Params& p, int g, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_rows_kernel<F>, p);
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
+template <int F>
+cudaError_t launch_form(const Params& p, int g, cudaStream_t stream) {
+  return launch_clusters(topk_rows_kernel<F>, p, p.batch, g, p.tie_cap, stream);
+}
+
+template <int F>
+cudaError_t launch_group_form(const GroupParams& gp, int g, cudaStream_t stream) {
+  return launch_clusters(topk_group_kernel<F>, gp, gp.row_begin[gp.n], g, gp.probs[0].tie_cap,
+                         stream);
+}
+
+template <class Kernel>
+cudaError_t prepare_kernel(Kernel kernel) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes(2, kTieCapMax)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 template <int F>
 cudaError_t prepare_form() {
-  cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<F>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes(2, kTieCapMax)));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topk_rows_kernel<F>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
+  return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F>) : e;
 }
 
 }  // namespace
@@ -1444,6 +1485,16 @@ cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream) {
     case kPaged: return launch_form<kPaged>(p, g, stream);
     case kRagged: return launch_form<kRagged>(p, g, stream);
     case kWindow: return launch_form<kWindow>(p, g, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream) {
+  switch (form) {
+    case kRaw: return launch_group_form<kRaw>(gp, g, stream);
+    case kPaged: return launch_group_form<kPaged>(gp, g, stream);
+    case kRagged: return launch_group_form<kRagged>(gp, g, stream);
+    case kWindow: return launch_group_form<kWindow>(gp, g, stream);
   }
   return cudaErrorInvalidValue;
 }

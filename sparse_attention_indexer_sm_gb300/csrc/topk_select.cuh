@@ -31,6 +31,16 @@ struct Params {
   int32_t use_filter;          // 1: try the sampled-threshold filter pass first
 };
 
+// Problems of one form sharing a launch (kMaxGroup at most; row_begin holds the
+// prefix sums of their batches, row_begin[n] = all rows). Passed by value as a
+// kernel parameter.
+constexpr int kMaxGroup = 32;
+struct GroupParams {
+  int32_t n;
+  int32_t row_begin[kMaxGroup + 1];
+  Params probs[kMaxGroup];
+};
+
 // Dynamic shared memory one CTA needs for a cluster of `g` CTAs.
 size_t smem_bytes(int g, int tie_cap);
 
@@ -39,5 +49,9 @@ cudaError_t prepare_device();
 
 // Enqueue the kernel: grid = batch * g CTAs in clusters of g along x.
 cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);
+
+// Enqueue one launch over every row of the group's problems (all of `form`, with
+// one tie capacity): grid = row_begin[n] * g CTAs in clusters of g.
+cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream);
 
 }  // namespace topk_gb300

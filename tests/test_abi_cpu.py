@@ -31,9 +31,10 @@ def lib():
     return pkg.load_library()
 
 
-def test_header_declares_the_three_forms():
+def test_header_declares_every_form():
     names = declared_functions()
     for n in ("topk_transform_raw", "topk_transform_paged", "topk_transform_ragged",
+              "topk_transform_window", "topk_transform_grouped", "topk_problem_bytes",
               "topk_workspace_bytes", "topk_status_string"):
         assert n in names
 
@@ -64,6 +65,37 @@ def test_host_side_argument_checks(lib):
     assert lib.topk_transform_ragged(one, None, one, 0, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_ragged(one, one, one, -1, 1, 16, one, None, 0, None) == 1
     assert lib.topk_workspace_bytes(256, 262144, 2048) == 0
+    assert lib.topk_transform_window(one, 8, None, one, 1, 16, one, None, 0, None) == 1
+    assert lib.topk_transform_window(one, 0, one, one, 1, 16, one, None, 0, None) == 1
+    assert lib.topk_transform_window(one, 8, one, one, 1, 0, one, None, 0, None) == 2
+
+
+def test_grouped_layout_and_host_checks(lib):
+    import sparse_attention_indexer_sm_gb300 as pkg
+    P = pkg.TopkProblem
+    assert lib.topk_problem_bytes() == ctypes.sizeof(P)
+    one = 16  # never dereferenced: every call below is rejected on the host
+
+    def group(*probs):
+        arr = (P * max(len(probs), 1))(*probs)
+        return lib.topk_transform_grouped(ctypes.addressof(arr), len(probs), None, 0, None)
+
+    ok_raw = P(form=0, batch=2, k=16, row_stride=64, scores=one, seq_lens=one, out=one)
+    assert lib.topk_transform_grouped(None, 0, None, 0, None) == 0        # nothing to do
+    assert lib.topk_transform_grouped(None, 1, None, 0, None) == 1        # null array
+    assert lib.topk_transform_grouped(None, -1, None, 0, None) == 1
+    assert lib.topk_transform_grouped(None, pkg.TOPK_MAX_GROUP + 1, None, 0, None) == 1
+    assert group(P(form=0, batch=0, k=16)) == 0                           # empty problems only
+    assert group(ok_raw, P(form=7, batch=1, k=16)) == 1                   # unknown form
+    assert group(ok_raw, P(form=0, batch=1, k=0, row_stride=8, scores=one, seq_lens=one,
+                           out=one)) == 2                                 # bad k, second problem
+    assert group(ok_raw, P(form=1, batch=1, k=4, row_stride=8, scores=one, seq_lens=one,
+                           out=one, page_size=64, page_table_stride=1)) == 1  # no page table
+    assert group(ok_raw, P(form=2, batch=1, k=4, scores=one, seq_lens=one, out=one)) == 1
+    assert group(ok_raw, P(form=3, batch=1, k=4, row_stride=8, scores=one, seq_lens=one,
+                           out=one)) == 1                                 # window without starts
+    assert group(P(form=0, batch=1, k=4, row_stride=8, scores=18, seq_lens=one,
+                   out=one)) == 1                                         # misaligned scores
 
 
 def test_tuning_controls_round_trip(lib):

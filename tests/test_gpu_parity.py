@@ -381,3 +381,83 @@ def test_window_from_zero_is_raw(pkg):
     ww = workloads.Workload("window_zero", "window", w.k, w.scores, w.seq_lens, None, 64,
                             np.zeros(w.batch, np.int32))
     assert same_sets(run_gpu(pkg, ww), run_gpu(pkg, w)).all()
+
+
+# ------------------------------------------------------------ grouped calls (several problems)
+
+def problem_of(w, dev):
+    """The device-side problem dict of one workload (for topk_transform_grouped)."""
+    q = {"form": w.form, "k": w.k,
+         "scores": torch.from_numpy(np.ascontiguousarray(w.scores)).to(dev),
+         "seq_lens": torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(dev),
+         "out": torch.full((w.batch, w.k), -7, dtype=torch.int32, device=dev)}
+    if w.form == "paged":
+        q["page_table"] = torch.from_numpy(np.ascontiguousarray(w.page_table)).to(dev)
+        q["page_size"] = w.page_size
+    elif w.form == "ragged":
+        q["row_starts"] = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
+        q["max_row_len_hint"] = int(np.max(w.seq_lens, initial=0))
+    elif w.form == "window":
+        q["starts"] = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
+    return q
+
+
+def run_grouped(pkg, ws):
+    dev = torch.device("cuda:0")
+    outs = pkg.topk_transform_grouped([problem_of(w, dev) for w in ws])
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in outs]
+
+
+def mixed_group():
+    g = np.random.Generator(np.random.PCG64(5))
+    raw = workloads.Workload("group_raw", "raw", 1024, workloads.random_rows(g, 8, 9001, "banded", True),
+                             g.integers(0, 9100, size=8).astype(np.int32))
+    small_k = workloads.config2(8192, batch=6)
+    small_k.k = 7
+    lens = g.integers(40000, 70000, size=3)
+    starts = np.concatenate([[5], 5 + np.cumsum(lens)[:-1]]).astype(np.int32)
+    packed = np.concatenate([workloads.row_values(g, "narrow", int(n), dup=True) for n in lens])
+    packed = np.concatenate([np.zeros(5, np.float32), packed]).astype(np.float32)
+    ragged = workloads.Workload("group_ragged", "ragged", 2048, packed, lens.astype(np.int32),
+                                None, 64, starts)
+    empty = workloads.Workload("group_empty", "raw", 16, np.zeros((0, 8), np.float32),
+                               np.zeros(0, np.int32))
+    return [workloads.config3(64), raw, workloads.prefill_windows(128, 8192, window=3000), ragged,
+            empty, small_k, workloads.config5(1)]
+
+
+def test_grouped_mixed_forms(pkg):
+    ws = mixed_group()
+    for w, got in zip(ws, run_grouped(pkg, ws)):
+        if w.batch:
+            assert_parity(w, got)
+
+
+@pytest.mark.parametrize("split,tie_cap,fast", [(4, None, None), (None, 64, None), (None, None, 0)])
+def test_grouped_settings(pkg, split, tie_cap, fast):
+    ws = mixed_group()[:4]
+    with settings(pkg, split=split, tie_cap=tie_cap, fast=fast):
+        outs = run_grouped(pkg, ws)
+    for w, got in zip(ws, outs):
+        assert_parity(w, got)
+
+
+def test_grouped_most_problems(pkg):
+    g = np.random.Generator(np.random.PCG64(9))
+    ws = []
+    for i in range(pkg.TOPK_MAX_GROUP):
+        B, stride = int(g.integers(1, 5)), int(g.integers(1000, 12000))
+        ws.append(workloads.Workload(f"group_{i}", "raw", int(g.integers(1, 2049)),
+                                     workloads.random_rows(g, B, stride, "normal"),
+                                     g.integers(0, stride + 10, size=B).astype(np.int32)))
+    for w, got in zip(ws, run_grouped(pkg, ws)):
+        assert_parity(w, got)
+    with pytest.raises(Exception):
+        run_grouped(pkg, ws + ws[:1])
+
+
+def test_grouped_equals_single_calls(pkg):
+    w = workloads.config3(128)
+    (got,) = run_grouped(pkg, [w])
+    assert same_sets(got, run_gpu(pkg, w)).all()
