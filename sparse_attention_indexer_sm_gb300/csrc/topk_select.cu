@@ -103,7 +103,7 @@ struct Ctl {
   uint32_t n_cand;                    // cand_cnt of CTA 0, broadcast
   uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
   uint32_t ns;                        // valid sample size (CTA 0)
-  uint32_t top_cnt;                   // candidates in the last candidate-histogram bin
+  uint32_t cls_cnt;                   // (winners, ties) slots of the candidate classification
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
@@ -327,8 +327,8 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
 // threshold bin for need1 (-> ctl.sel_*) and, if `two`, for need2 (-> ctl.sel2_*):
 // the bin where the count from the top reaches need (1 <= need <= sum of h). Lane
 // l first sums bins [32 l, 32 l + 32) (reads of 32 distinct banks, padded layout);
-// a suffix scan over the lanes names the lane whose range holds the threshold, and
-// the warp then scans that lane's 32 bins, one per lane. The results are visible
+// a suffix scan over the lanes names the lane whose range holds each threshold,
+// and the warp then scans that lane's 32 bins, one per lane, for both needs at once. The results are visible
 // to the block after the caller's next barrier.
 __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, uint32_t need2,
                                            bool two, Ctl& ctl) {
@@ -343,35 +343,37 @@ __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, ui
     if (lane + off < 32) x += y;
   }
   const uint32_t excl = x - s;  // count in the bins of lanes > lane
+  // both searches in the same instructions (their latencies overlap)
+  const uint32_t n2 = two ? need2 : need1;
+  const uint32_t hit1 = __ballot_sync(kFull, s != 0 && excl < need1 && need1 <= x);
+  const uint32_t hit2 = __ballot_sync(kFull, s != 0 && excl < n2 && n2 <= x);
+  if (hit1 == 0u || hit2 == 0u) return;  // a need outside [1, sum]: nothing to find
+  const int o1 = __ffs(hit1) - 1, o2 = __ffs(hit2) - 1;
+  const uint32_t above1 = __shfl_sync(kFull, excl, o1), above2 = __shfl_sync(kFull, excl, o2);
+  const int b1 = o1 * 32 + lane, b2 = o2 * 32 + lane;
+  const uint32_t c1 = h[hist_index(b1)], c2 = h[hist_index(b2)];
+  uint32_t y1 = c1, y2 = c2;  // counts in the owner's bins >= b
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    if (q == 1 && !two) break;
-    const uint32_t need = q == 0 ? need1 : need2;
-    const uint32_t hit = __ballot_sync(kFull, s != 0 && excl < need && need <= x);
-    if (hit == 0u) continue;  // need outside [1, sum]: nothing to find
-    const int owner = __ffs(hit) - 1;
-    const uint32_t owner_above = __shfl_sync(kFull, excl, owner);
-    const int b = owner * 32 + lane;
-    const uint32_t c = h[hist_index(b)];
-    uint32_t y = c;  // count in the owner's bins >= b
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t z = __shfl_down_sync(kFull, y, off);
-      if (lane + off < 32) y += z;
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t z1 = __shfl_down_sync(kFull, y1, off);
+    const uint32_t z2 = __shfl_down_sync(kFull, y2, off);
+    if (lane + off < 32) {
+      y1 += z1;
+      y2 += z2;
     }
-    const uint32_t above = owner_above + y - c;
-    const uint32_t here = __ballot_sync(kFull, c != 0 && above < need && need <= above + c);
-    if (here != 0u && lane == __ffs(here) - 1) {
-      if (q == 0) {
-        ctl.sel_t = static_cast<uint32_t>(b);
-        ctl.sel_above = above;
-        ctl.sel_count = c;
-      } else {
-        ctl.sel2_t = static_cast<uint32_t>(b);
-        ctl.sel2_above = above;
-        ctl.sel2_count = c;
-      }
-    }
+  }
+  const uint32_t a1 = above1 + y1 - c1, a2 = above2 + y2 - c2;
+  const uint32_t here1 = __ballot_sync(kFull, c1 != 0 && a1 < need1 && need1 <= a1 + c1);
+  const uint32_t here2 = __ballot_sync(kFull, c2 != 0 && a2 < n2 && n2 <= a2 + c2);
+  if (here1 != 0u && lane == __ffs(here1) - 1) {
+    ctl.sel_t = static_cast<uint32_t>(b1);
+    ctl.sel_above = a1;
+    ctl.sel_count = c1;
+  }
+  if (two && here2 != 0u && lane == __ffs(here2) - 1) {
+    ctl.sel2_t = static_cast<uint32_t>(b2);
+    ctl.sel2_above = a2;
+    ctl.sel2_count = c2;
   }
 }
 
@@ -633,8 +635,12 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
       // four standard deviations on lambda's side (a lambda above the k-th key
       // costs the exact tier: about 3e-5 of rows), three on the other (it only sets
       // the candidate-histogram bin width)
-      const float mean = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(L);
-      const float sd = sqrtf(mean);
+      // (approximate arithmetic is enough: any ranks give an exact result, these
+      // only make the fast tier likely)
+      const float mean =
+          fmaxf(__fdividef(static_cast<float>(k) * static_cast<float>(ns), static_cast<float>(L)),
+                1.0f);
+      const float sd = mean * rsqrtf(mean);
       rs = static_cast<uint32_t>(ceilf(mean + 4.0f * sd)) + 2u;
       if (rs > ns) rs = ns;
       const float lo = floorf(mean - 3.0f * sd);
@@ -731,9 +737,10 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
 // F2, a row owned by one CTA: stream the row, keep per lane a 32-bit candidate
 // mask per iteration (8 quads), and every kMaskIters iterations turn the masks into
 // positions written compactly into the buffer (entry .y; .x is filled by
-// fill_candidates) at slots from one block-wide prefix count per group. Holding
-// only masks lets the loads of a whole group be in flight together. Slots at or
-// beyond `cap` are counted but not written.
+// fill_candidates) at slots from one reservation per warp and group on the CTA's
+// counter (ctl.cand_cnt, zero on entry). Holding only masks lets the loads of a
+// whole group be in flight together. Slots at or beyond `cap` are counted but not
+// written.
 template <bool kPos>
 __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint2* buf,
                                                  uint32_t cap, Ctl& ctl) {
@@ -745,7 +752,6 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
   int32_t ej;
   const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
   bool first = true;
-  uint32_t running = 0;  // candidates so far
   for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
     uint32_t mk[MI];
 #pragma unroll
@@ -774,11 +780,8 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     uint32_t n = with_edge ? 1u : 0u;
 #pragma unroll
     for (int it = 0; it < MI; ++it) n += static_cast<uint32_t>(__popc(mk[it]));
-    uint32_t total;
-    const uint32_t off = block_excl_scan(n, ctl, &total);
-    if (total != 0) {
-      uint32_t slot = running + off;
-      running += total;
+    uint32_t slot = warp_reserve(&ctl.cand_cnt, 0u, false, n);
+    {
       auto put = [&](int32_t j) {
         if (slot < cap) buf[slot].y = static_cast<uint32_t>(j);
         ++slot;
@@ -797,7 +800,6 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     }
     first = false;
   }
-  if (tid == 0) ctl.cand_cnt = running;
 }
 
 // F2, a row owned by one CTA: the n buffered positions get their keys, read back
@@ -830,11 +832,10 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
         if (!top) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
       }
       const uint32_t b = __ballot_sync(kFull, top);
-      if ((tid & 31) == 0 && b != 0) atomicAdd(&ctl.top_cnt, static_cast<uint32_t>(__popc(b)));
+      if ((tid & 31) == 0 && b != 0)
+        atomicAdd(&chist[hist_index(kFastBins - 1)], static_cast<uint32_t>(__popc(b)));
     }
   }
-  __syncthreads();
-  if (tid == 0) chist[hist_index(kFastBins - 1)] = ctl.top_cnt;
   __syncthreads();
 }
 
@@ -996,8 +997,8 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
     return;
   }
   // candidates above the threshold bin are winners; the bin's go to the list. Each
-  // thread takes entries tid, tid + kThreads, ...; one block-wide prefix count of
-  // (winners, ties), packed in one word, gives every slot.
+  // thread takes entries tid, tid + kThreads, ...; one reservation per warp of
+  // (winners, ties), packed in one word of ctl.cls_cnt, gives every slot.
   constexpr int kPer = kTieCapMax / kThreads;
   uint32_t cls = 0;  // bit 2r: winner, bit 2r+1: tie, for entry tid + r * kThreads
   uint32_t nw = 0, nt = 0;
@@ -1015,8 +1016,7 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
       }
     }
   }
-  uint32_t total;
-  const uint32_t off = block_excl_scan(nw | (nt << 16), ctl, &total);
+  const uint32_t off = warp_reserve(&ctl.cls_cnt, 0u, false, nw | (nt << 16));
   uint32_t ws = off & 0xFFFFu, ts = off >> 16;
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
@@ -1184,7 +1184,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     ctl.out_cnt = 0;
     ctl.cand_cnt = 0;
     ctl.ns = 0;
-    ctl.top_cnt = 0;
+    ctl.cls_cnt = 0;
     ctl.lambda = 0;
     ctl.lambda_shift = 0;
   }
