@@ -497,11 +497,15 @@ __device__ __forceinline__ void visit_keys(const Slice& s, F&& f) {
   }
 }
 
-// Bulk L2 prefetch of a slice's aligned body, in 16 KB pieces over the threads.
-__device__ __forceinline__ void prefetch_slice(const Slice& s) {
+// Bulk L2 prefetch of a slice's aligned body, in 16 KB pieces over the threads
+// from `first` on (the issuing threads wait while the copy engine's queue is full,
+// so the caller picks threads that are not on the critical path).
+__device__ __forceinline__ void prefetch_slice(const Slice& s, int first = 0) {
   const uint64_t bytes = 16ull * static_cast<uint64_t>(s.nq);
   const uint64_t pieces = (bytes + kPrefetchBytes - 1) / kPrefetchBytes;
-  for (uint64_t i = threadIdx.x; i < pieces; i += kThreads)
+  const int t = static_cast<int>(threadIdx.x) - first;
+  if (t < 0) return;
+  for (uint64_t i = static_cast<uint64_t>(t); i < pieces; i += static_cast<uint64_t>(kThreads - first))
     prefetch_l2(reinterpret_cast<const char*>(s.vec) + i * kPrefetchBytes,
                 static_cast<uint32_t>(min(static_cast<uint64_t>(kPrefetchBytes),
                                           bytes - i * kPrefetchBytes)));
@@ -615,7 +619,6 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
       atomicAdd(&hist[kH1 + hist_index(static_cast<int>(bin))], static_cast<uint32_t>(__popc(peers)));
     mine += v ? 1u : 0u;
   }
-  prefetch_slice(s);  // the sample has arrived: now the bulk of the slice
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(kFull, mine, off);
   if ((tid & 31) == 0 && mine != 0) {
@@ -626,6 +629,9 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist + kH1, mhist + kH1, kFastWords);
+  // the sample has arrived: now the bulk of the slice, issued by the last warp while
+  // the first one looks for the thresholds
+  prefetch_slice(s, kThreads - 32);
   // sample ranks a few standard deviations either side of the expected sample rank
   // of the row's k-th key
   uint32_t rs = 0, rs_lo = 0;
