@@ -606,9 +606,9 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
                                                   uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
   const int tid = threadIdx.x;
   const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
-  // round 1: coarse bins (top 10 key bits), one shared atomic per sample key (same-
-  // bin atomics of a warp are merged by the hardware; this measured faster than
-  // aggregating them with a match first). The valid sample size goes to CTA 0.
+  // round 1: coarse bins (top 10 key bits), one shared atomic per sample key (this
+  // measured faster than first aggregating a warp's equal bins with a match). The
+  // valid sample size goes to CTA 0.
   uint32_t mine = 0;
 #pragma unroll
   for (int i = 0; i < 4 * kSampleQuads; ++i) {
