@@ -1177,8 +1177,26 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   uint2* buf = reinterpret_cast<uint2*>(dyn + (G > 1 ? 3 : 2) * kHistWords + kPtCap);
   const uint32_t cap = static_cast<uint32_t>(p.tie_cap);
 
-  // independent of the row: clear the histograms and counters while the row's
-  // length is being read
+  // the row's length (and start) first: everything waits for them
+  const int32_t seq = p.seq_lens[row];
+  int32_t start = 0;  // ragged: row offset; window: window start
+  if constexpr (F == kRagged || F == kWindow) start = p.row_starts[row];
+  // raw, paged: the row's start does not depend on its length, so the sample is
+  // loaded (over the whole row stride; elements at or past the length are ignored
+  // later) while the length is still on its way
+  Sample sm;
+  bool sample_loaded = false;
+  if constexpr (F == kRaw || F == kPaged) {
+    if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
+      load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
+                             static_cast<int32_t>(p.row_stride), rank, G),
+                  sm);
+      sample_loaded = true;
+    }
+  }
+
+  // independent of the row: clear the histograms and counters while those loads
+  // are in flight
   for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
   if (G > 1 && rank == 0)
     for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
@@ -1199,29 +1217,15 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   m.ps = p.page_size;
   m.ps_shift = p.page_shift;
   m.rstart = 0;
-  const int32_t seq = p.seq_lens[row];
   const float* rowp;
   int32_t L;
-  // raw, paged: the row's start does not depend on its length, so the sample is
-  // loaded (over the whole row stride; elements at or past the length are ignored
-  // later) while the length is still on its way
-  Sample sm;
-  bool sample_loaded = false;
-  if constexpr (F == kRaw || F == kPaged) {
-    if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
-      load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
-                             static_cast<int32_t>(p.row_stride), rank, G),
-                  sm);
-      sample_loaded = true;
-    }
-  }
   if constexpr (F == kRagged) {
-    m.rstart = p.row_starts[row];
+    m.rstart = start;
     rowp = p.scores + m.rstart;
     L = max(seq, 0);
   } else if constexpr (F == kWindow) {  // columns [lo, hi) of the row, clamped to it
     const int64_t hi = min(static_cast<int64_t>(max(seq, 0)), p.row_stride);
-    const int64_t lo = min(static_cast<int64_t>(max(p.row_starts[row], 0)), hi);
+    const int64_t lo = min(static_cast<int64_t>(max(start, 0)), hi);
     m.rstart = static_cast<int32_t>(lo);
     rowp = p.scores + static_cast<int64_t>(row) * p.row_stride + lo;
     L = static_cast<int32_t>(hi - lo);
@@ -1248,7 +1252,8 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // of a cluster, and rows of more than kPtCap pages, read it from global memory
   int32_t pages = 0;
   if constexpr (F == kPaged) {
-    const int64_t np = (static_cast<int64_t>(L) + p.page_size - 1) / p.page_size;
+    const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
+    const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
     if (rank == 0 && np <= kPtCap) {
       pages = static_cast<int32_t>(np);
       for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, m.pt_row + i);
