@@ -219,8 +219,8 @@ def call(pkg, w, d, stream):
         pkg.topk_transform_paged(d["scores"], d["seq"], d["pt"], w.page_size, w.k, out=d["out"],
                                  stream=stream)
     elif w.form == "window":
-        pkg.topk_transform_window(d["scores"], d["starts"], d["seq"], w.k, out=d["out"],
-                                  stream=stream)
+        pkg.topk_transform_window(d["scores"], d["starts"], d["seq"], w.k,
+                                  max_row_len_hint=w.max_row_len, out=d["out"], stream=stream)
     else:
         pkg.topk_transform_raw(d["scores"], d["seq"], w.k, out=d["out"], stream=stream)
 

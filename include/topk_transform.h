@@ -117,10 +117,13 @@ int topk_transform_ragged(const float* scores, const int32_t* row_starts,
 /* Window form: row b of scores [batch, row_stride] selects among its columns
  * [starts[b], seq_lens[b]) (both clamped to [0, row_stride]; an empty window if
  * the end is not after the start) and writes the selected columns. With every
- * start 0 it is the raw form. row_stride >= 1; starts, seq_lens [batch]. */
+ * start 0 it is the raw form. row_stride >= 1; starts, seq_lens [batch].
+ * max_row_len_hint (>= 0) is an upper bound of the window lengths, used only to
+ * choose the kernel configuration; 0 means row_stride. */
 int topk_transform_window(const float* scores, int64_t row_stride, const int32_t* starts,
-                          const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
-                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                          const int32_t* seq_lens, int64_t max_row_len_hint, int32_t batch,
+                          int32_t k, int32_t* out, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
 
 /* ------------------------------------------------------------------ grouped calls
  *
@@ -140,7 +143,7 @@ typedef enum {
 /* One problem: the arguments of its form's entry point. Fields a form does not
  * use are ignored (row_stride: raw, paged, window; page_table, page_table_stride,
  * page_size: paged; row_starts: ragged row offsets or window starts;
- * max_row_len_hint: ragged). */
+ * max_row_len_hint: ragged and window, as for their entry points). */
 typedef struct {
   int32_t form;               /* topk_form_t */
   int32_t batch;              /* rows, >= 0 (0: nothing to do) */
@@ -193,11 +196,19 @@ int topk_last_cuda_error(void);
  *
  * topk_set_fast_tier(enable): 1 (default) first tries the one-pass filter whose
  * threshold comes from a sample of the row and is verified afterwards; 0 always
- * runs the exact histogram tier. The result is the same either way. */
+ * runs the exact histogram tier. The result is the same either way.
+ *
+ * topk_set_cta_threads(t): which build of the kernels runs: 512-thread CTAs (two
+ * per SM) or 256-thread CTAs (four per SM, at most 3072 tie-buffer entries); any
+ * other value restores the built-in choice, which takes the 256-thread build for
+ * launches of more rows than two CTAs per SM hold, rows of at most 16384 elements
+ * (by row_stride, or the ragged hint), one CTA per row and k <= 1024.
+ * The result is the same either way. */
 #define TOPK_TIE_CAPACITY_MAX 4096
 int topk_set_row_split(int g);
 int topk_set_tie_capacity(int cap);
 int topk_set_fast_tier(int enable);
+int topk_set_cta_threads(int threads);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
     "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged", "topk_transform_window",
-    "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP",
+    "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "topk_set_cta_threads",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
@@ -69,7 +69,7 @@ def load_library() -> ctypes.CDLL:
             lib.topk_transform_ragged.restype = ctypes.c_int
             lib.topk_transform_ragged.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, sz, vp]
             lib.topk_transform_window.restype = ctypes.c_int
-            lib.topk_transform_window.argtypes = [vp, i64, vp, vp, i32, i32, vp, vp, sz, vp]
+            lib.topk_transform_window.argtypes = [vp, i64, vp, vp, i64, i32, i32, vp, vp, sz, vp]
             lib.topk_transform_grouped.restype = ctypes.c_int
             lib.topk_transform_grouped.argtypes = [vp, i32, vp, sz, vp]
             lib.topk_problem_bytes.restype = sz
@@ -85,6 +85,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_set_row_split.argtypes = [ctypes.c_int]
             lib.topk_set_tie_capacity.restype = ctypes.c_int
             lib.topk_set_tie_capacity.argtypes = [ctypes.c_int]
+            lib.topk_set_cta_threads.restype = ctypes.c_int
+            lib.topk_set_cta_threads.argtypes = [ctypes.c_int]
             lib.topk_set_fast_tier.restype = ctypes.c_int
             lib.topk_set_fast_tier.argtypes = [ctypes.c_int]
             _lib = lib
@@ -207,9 +209,12 @@ def topk_transform_ragged(scores: torch.Tensor, row_starts: torch.Tensor, seq_le
 
 
 def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: torch.Tensor,
-                          k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                          k: int, max_row_len_hint: int = 0, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
     """Exact top-k of each row's window of columns [starts[b], seq_lens[b]) (both
-    clamped to the row); the selected columns are written."""
+    clamped to the row); the selected columns are written. max_row_len_hint: an
+    upper bound of the window lengths (0: the row length), used only to pick the
+    kernel configuration."""
     lib = load_library()
     batch, row_stride = _scores_2d(scores)
     dev = scores.device
@@ -218,8 +223,8 @@ def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: 
     out = _out(out, batch, k, dev)
     with torch.cuda.device(dev):
         st = lib.topk_transform_window(scores.data_ptr(), row_stride, starts.data_ptr(),
-                                       seq_lens.data_ptr(), batch, k, out.data_ptr(), None, 0,
-                                       _stream(stream, dev))
+                                       seq_lens.data_ptr(), int(max_row_len_hint), batch, k,
+                                       out.data_ptr(), None, 0, _stream(stream, dev))
     _check(st, "topk_transform_window")
     return out
 
@@ -243,8 +248,8 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
 
     Each problem is a dict with "form" ("raw", "paged", "ragged" or "window"), "k",
     "scores", "seq_lens" and what its form needs: "page_table" and "page_size"
-    (paged), "row_starts" and optionally "max_row_len_hint" (ragged), "starts"
-    (window); "out" is optional. Returns the output tensors, in order."""
+    (paged), "row_starts" and optionally "max_row_len_hint" (ragged), "starts" and
+    optionally "max_row_len_hint" (window); "out" is optional. Returns the output tensors, in order."""
     lib = load_library()
     if len(problems) > TOPK_MAX_GROUP:
         raise ValueError(f"at most {TOPK_MAX_GROUP} problems per grouped call")
@@ -288,6 +293,7 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
         elif form == "window":
             _vector(q["starts"], "starts", batch, d)
             arr[i].row_starts = q["starts"].data_ptr()
+            arr[i].max_row_len_hint = int(q.get("max_row_len_hint", 0))
         out = _out(q.get("out"), batch, k, d)
         arr[i].form, arr[i].batch, arr[i].k = _FORMS[form], batch, k
         arr[i].scores, arr[i].seq_lens, arr[i].out = scores.data_ptr(), q["seq_lens"].data_ptr(), out.data_ptr()
@@ -309,6 +315,12 @@ def topk_set_row_split(g: int) -> int:
 def topk_set_tie_capacity(cap: int) -> int:
     """Entries of the shared tie buffer (0 .. TOPK_TIE_CAPACITY_MAX); for tests."""
     return int(load_library().topk_set_tie_capacity(int(cap)))
+
+
+def topk_set_cta_threads(threads: int) -> int:
+    """Which kernel build runs: 512 or 256 threads per CTA; anything else restores
+    the built-in choice (returned as 0)."""
+    return int(load_library().topk_set_cta_threads(int(threads)))
 
 
 def topk_set_fast_tier(enable: bool) -> int:

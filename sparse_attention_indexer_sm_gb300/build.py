@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libtopk_transform.so")
 
-SOURCES = ("topk_select.cu", "topk_api.cu")
+SOURCES = ("topk_select.cu", "topk_select_cta256.cu", "topk_api.cu")
 HEADERS = (os.path.join(CSRC, "topk_select.cuh"), os.path.join(INCLUDE, "topk_transform.h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -2,6 +2,7 @@
 // CTAs share a row, per-device set-up, and the launch. See
 // include/topk_transform.h for the contract of every entry point.
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstdlib>
@@ -21,6 +22,7 @@ constexpr int kRowSplitUnset = INT_MIN;
 std::atomic<int> g_row_split{kRowSplitUnset};
 std::atomic<int> g_tie_cap{topk_gb300::kTieCapMax};
 std::atomic<int> g_fast_tier{1};
+std::atomic<int> g_cta_threads{0};  // 0: automatic; 512 or 256: that build
 thread_local int t_last_cuda_error = 0;
 
 struct DeviceState {
@@ -69,6 +71,19 @@ int choose_split(int64_t batch, int64_t row_len, int sm_count) {
   return g >= 4 ? g : 1;
 }
 
+// Launches of more rows than two 512-thread CTAs per SM hold take the 256-thread
+// build (four CTAs per SM, so each SM overlaps more rows) when one CTA owns a row,
+// the rows are at most 16384 elements (measured: faster at 8192, even at 16384,
+// slower at 32768, where half the threads per row lengthen each row's chain more
+// than the extra rows hide) and every problem's candidates fit that build's
+// smaller buffer (k <= 1024). row_len <= 0 means unknown.
+bool use_cta256(int64_t rows, int64_t row_len, int g, int32_t k_max, int sm_count) {
+  const int forced = g_cta_threads.load(std::memory_order_relaxed);
+  if (forced != 0) return forced == 256;
+  return g == 1 && rows > 2 * static_cast<int64_t>(sm_count) && k_max <= 1024 &&
+         row_len > 0 && row_len <= 16384;
+}
+
 int fail_cuda(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
   return TOPK_ERR_CUDA;
@@ -83,7 +98,8 @@ int device_state(DeviceState** out) {
   DeviceState& ds = g_devices[dev];
   std::call_once(ds.once, [&ds, dev]() {
     ds.err = cudaDeviceGetAttribute(&ds.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (ds.err == cudaSuccess) ds.err = topk_gb300::prepare_device();
+    if (ds.err == cudaSuccess) ds.err = topk_gb300::cta512::prepare_device();
+    if (ds.err == cudaSuccess) ds.err = topk_gb300::cta256::prepare_device();
   });
   if (ds.err != cudaSuccess) return fail_cuda(ds.err);
   *out = &ds;
@@ -126,8 +142,10 @@ int build_params(const topk_problem_t& q, Params* p, int64_t* len_hint) {
     p->page_size = q.page_size;
     p->page_shift = (q.page_size & (q.page_size - 1)) == 0 ? __builtin_ctz(q.page_size) : -1;
   } else if (q.form == TOPK_FORM_WINDOW) {
-    if (q.row_starts == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+    if (q.row_starts == nullptr || q.max_row_len_hint < 0) return TOPK_ERR_INVALID_ARGUMENT;
     p->row_starts = q.row_starts;
+    if (q.max_row_len_hint > 0 && q.max_row_len_hint < q.row_stride)
+      *len_hint = q.max_row_len_hint;
   }
   return TOPK_OK;
 }
@@ -157,7 +175,13 @@ int run_one(const topk_problem_t& q, cudaStream_t stream) {
   const int g = choose_split(p.batch, hint, ds->sm_count);
   if (static_cast<int64_t>(p.batch) * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
   apply_settings(settings(), &p);
-  const cudaError_t e = topk_gb300::launch(static_cast<Form>(q.form), p, g, stream);
+  cudaError_t e;
+  if (use_cta256(p.batch, hint, g, p.k, ds->sm_count)) {
+    p.tie_cap = std::min(p.tie_cap, topk_gb300::kTieCap256);
+    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, stream);
+  } else {
+    e = topk_gb300::cta512::launch(static_cast<Form>(q.form), p, g, stream);
+  }
   return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
 }
 
@@ -212,10 +236,12 @@ int topk_transform_ragged(const float* scores, const int32_t* row_starts,
 }
 
 int topk_transform_window(const float* scores, int64_t row_stride, const int32_t* starts,
-                          const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
-                          void* /*workspace*/, size_t /*workspace_bytes*/, cudaStream_t stream) {
+                          const int32_t* seq_lens, int64_t max_row_len_hint, int32_t batch,
+                          int32_t k, int32_t* out, void* /*workspace*/,
+                          size_t /*workspace_bytes*/, cudaStream_t stream) {
   topk_problem_t q = problem(TOPK_FORM_WINDOW, scores, row_stride, seq_lens, batch, k, out);
   q.row_starts = starts;
+  q.max_row_len_hint = max_row_len_hint;
   return run_one(q, stream);
 }
 
@@ -260,7 +286,16 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     const int g = choose_split(rows, hint < 0 ? 0 : hint, ds->sm_count);
     if (rows * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
     gp.row_begin[gp.n] = static_cast<int32_t>(rows);
-    const cudaError_t e = topk_gb300::launch_group(static_cast<Form>(f), gp, g, stream);
+    int32_t k_max = 0;
+    for (int i = 0; i < gp.n; ++i) k_max = std::max(k_max, gp.probs[i].k);
+    cudaError_t e;
+    if (use_cta256(rows, hint, g, k_max, ds->sm_count)) {
+      for (int i = 0; i < gp.n; ++i)
+        gp.probs[i].tie_cap = std::min(gp.probs[i].tie_cap, topk_gb300::kTieCap256);
+      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, stream);
+    } else {
+      e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, stream);
+    }
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return TOPK_OK;
@@ -287,6 +322,11 @@ int topk_set_row_split(int g) {
 
 int topk_set_fast_tier(int enable) {
   return g_fast_tier.exchange(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+}
+
+int topk_set_cta_threads(int threads) {
+  return g_cta_threads.exchange(threads == 512 || threads == 256 ? threads : 0,
+                                std::memory_order_relaxed);
 }
 
 int topk_set_tie_capacity(int cap) {

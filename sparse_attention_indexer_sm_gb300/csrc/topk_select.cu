@@ -61,18 +61,39 @@
 
 #include "topk_select.cuh"
 
+// This file is compiled twice: with TOPK_CTA_THREADS = 512 (namespace cta512: two
+// CTAs per SM, every launch that fits one wave) and 256 (cta256: four CTAs per SM,
+// for launches of more rows than that, so that each SM overlaps four rows'
+// latency chains instead of two).
+#ifndef TOPK_CTA_THREADS
+#define TOPK_CTA_THREADS 512
+#endif
+#if TOPK_CTA_THREADS == 512
+#define TOPK_CTA_NS cta512
+#elif TOPK_CTA_THREADS == 256
+#define TOPK_CTA_NS cta256
+#else
+#error "TOPK_CTA_THREADS must be 512 or 256"
+#endif
+
 namespace topk_gb300 {
+namespace TOPK_CTA_NS {
 namespace {
 
+constexpr int kThreads = TOPK_CTA_THREADS;  // threads per CTA
+constexpr int kCtasPerSm = 1024 / kThreads;  // at 64 registers per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;            // 128-bit loads in flight per thread per step (exact tier)
 constexpr int kFilterUnroll = 8;      // 128-bit loads in flight per thread in the filter
 constexpr int kMaskIters = 4;         // filter iterations whose masks are decoded together
 constexpr int kRowRoundBits = 12;     // histogram width of the rounds over the row
 constexpr int kBufRoundBits = 12;     // histogram width of the rounds over a buffer
-constexpr int kSampleQuads = 1;       // sampled 16-byte quads per thread
+constexpr int kSampleQuads = 512 / kThreads;  // sampled 16-byte quads per thread (2048 keys per CTA)
 constexpr uint32_t kPrefetchBytes = 16384;  // one bulk L2 prefetch
-constexpr int kPtCap = 4096;          // page-table entries staged in shared memory
+// page-table entries staged in shared memory (rows with more pages read the table
+// from global memory); the 256-thread build keeps its shared memory within a
+// quarter of the SM's
+constexpr int kPtCap = kThreads == 512 ? 4096 : 1024;
 constexpr int kRankDirect = 64;       // threshold bins this small are ordered by rank count
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -81,7 +102,11 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // memory bank conflicts.
 __host__ __device__ constexpr int hist_index(int b) { return b + (b >> 5); }
 constexpr int kHistWords = hist_index(kMaxBins);
-constexpr int kListCap = kHistWords / 2;  // (key, position) entries of the list region
+// (key, position) entries of the list region (the candidates of the threshold bin;
+// a bin holding more is refined in the candidate buffer instead). The 256-thread
+// build keeps a short list to give its candidate buffer room.
+constexpr int kListCap = kThreads == 512 ? kHistWords / 2 : 512;
+constexpr int kListWords = 2 * kListCap;
 
 // The fast tier's histograms have 1024 bins, small enough for one warp to find a
 // threshold in (no block-wide scan). Each has its own region of `hist` (and, in
@@ -807,7 +832,7 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
 }
 
 // F2, a row owned by one CTA: the n buffered positions get their keys, read back
-// (from L2) in batches of four per thread, and the candidate histogram (bin =
+// (from L2) in batches of 2048, and the candidate histogram (bin =
 // min((key - lambda) >> shift, kFastBins - 1)) is counted in `chist`, which is zero
 // on entry. The last
 // bin collects most candidates, so it is counted per warp (ballot) rather than by
@@ -816,17 +841,20 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
                                                 uint32_t lambda, uint32_t shift,
                                                 uint32_t* chist, Ctl& ctl) {
   const int tid = threadIdx.x;
+  // 2048 candidates per batch whatever the CTA size: one L2 round trip for the
+  // candidate counts the fast tier normally sees
+  constexpr int kPer = 2048 / kThreads;
   // the loop bound is the same for every thread (the ballot below needs whole warps)
-  for (uint32_t base = 0; base < n; base += 4 * kThreads) {
+  for (uint32_t base = 0; base < n; base += kPer * kThreads) {
     const uint32_t i0 = base + static_cast<uint32_t>(tid);
-    uint32_t bits[4];
+    uint32_t bits[kPer];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kPer; ++r) {
       const uint32_t i = i0 + r * kThreads;
       bits[r] = i < n ? __float_as_uint(__ldg(row + buf[i].y)) : 0u;
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kPer; ++r) {
       const uint32_t i = i0 + r * kThreads;
       const uint32_t key = order_key(bits[r]);
       const uint32_t d = (key - lambda) >> shift;
@@ -1172,9 +1200,10 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // candidate/tie buffer
   uint32_t* hist = dyn;
   uint2* list = reinterpret_cast<uint2*>(dyn + kHistWords);
-  int32_t* pt_smem = reinterpret_cast<int32_t*>(dyn + 2 * kHistWords);
-  uint32_t* mhist = dyn + 2 * kHistWords + kPtCap;
-  uint2* buf = reinterpret_cast<uint2*>(dyn + (G > 1 ? 3 : 2) * kHistWords + kPtCap);
+  int32_t* pt_smem = reinterpret_cast<int32_t*>(dyn + kHistWords + kListWords);
+  uint32_t* mhist = dyn + kHistWords + kListWords + kPtCap;
+  uint2* buf =
+      reinterpret_cast<uint2*>(dyn + (G > 1 ? 2 : 1) * kHistWords + kListWords + kPtCap);
   const uint32_t cap = static_cast<uint32_t>(p.tie_cap);
 
   // the row's length (and start) first: everything waits for them
@@ -1404,7 +1433,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
 
 // One cluster of G CTAs per row.
 template <int F>
-__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_rows_kernel(const Params p) {
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Ctl ctl;
   const int G = static_cast<int>(cluster_nctarank());
@@ -1416,7 +1445,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 // in order (problem i owns rows [row_begin[i], row_begin[i + 1])). Each CTA copies
 // its problem's parameters to shared memory once.
 template <int F>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     topk_group_kernel(const __grid_constant__ GroupParams gp) {
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Ctl ctl;
@@ -1476,7 +1505,7 @@ cudaError_t prepare_form() {
 }  // namespace
 
 size_t smem_bytes(int g, int tie_cap) {
-  return sizeof(uint32_t) * (kHistWords * (g > 1 ? 3 : 2) + kPtCap) +
+  return sizeof(uint32_t) * (kHistWords * (g > 1 ? 2 : 1) + kListWords + kPtCap) +
          sizeof(uint2) * static_cast<size_t>(tie_cap);
 }
 
@@ -1508,4 +1537,5 @@ cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t s
   return cudaErrorInvalidValue;
 }
 
+}  // namespace TOPK_CTA_NS
 }  // namespace topk_gb300

@@ -10,7 +10,6 @@ namespace topk_gb300 {
 
 enum Form : int { kRaw = 0, kPaged = 1, kRagged = 2, kWindow = 3 };
 
-constexpr int kThreads = 512;          // threads per CTA
 constexpr int kMaxBins = 4096;         // widest histogram (12 key bits)
 constexpr int kTieCapMax = 4096;       // shared tie buffer entries, 8 bytes each
 constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
@@ -41,17 +40,28 @@ struct GroupParams {
   Params probs[kMaxGroup];
 };
 
-// Dynamic shared memory one CTA needs for a cluster of `g` CTAs.
-size_t smem_bytes(int g, int tie_cap);
+// The kernels are built twice (topk_select.cu): cta512 has 512-thread CTAs, two per
+// SM; cta256 has 256-thread CTAs, four per SM, and takes tie capacities up to
+// kTieCap256 only. Each build exports the same functions.
+constexpr int kTieCap256 = 3072;
 
-// One-time per-device function attributes (max dynamic smem, cluster size 16).
-cudaError_t prepare_device();
+#define TOPK_CTA_INTERFACE                                                              \
+  /* Dynamic shared memory one CTA needs for a cluster of `g` CTAs. */                  \
+  size_t smem_bytes(int g, int tie_cap);                                                \
+  /* One-time per-device function attributes (max dynamic smem, cluster size 16). */    \
+  cudaError_t prepare_device();                                                         \
+  /* Enqueue the kernel: grid = batch * g CTAs in clusters of g along x. */             \
+  cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);           \
+  /* Enqueue one launch over every row of the group's problems (all of `form`, with */  \
+  /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. */               \
+  cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream);
 
-// Enqueue the kernel: grid = batch * g CTAs in clusters of g along x.
-cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);
-
-// Enqueue one launch over every row of the group's problems (all of `form`, with
-// one tie capacity): grid = row_begin[n] * g CTAs in clusters of g.
-cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream);
+namespace cta512 {
+TOPK_CTA_INTERFACE
+}
+namespace cta256 {
+TOPK_CTA_INTERFACE
+}
+#undef TOPK_CTA_INTERFACE
 
 }  // namespace topk_gb300

@@ -65,9 +65,10 @@ def test_host_side_argument_checks(lib):
     assert lib.topk_transform_ragged(one, None, one, 0, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_ragged(one, one, one, -1, 1, 16, one, None, 0, None) == 1
     assert lib.topk_workspace_bytes(256, 262144, 2048) == 0
-    assert lib.topk_transform_window(one, 8, None, one, 1, 16, one, None, 0, None) == 1
-    assert lib.topk_transform_window(one, 0, one, one, 1, 16, one, None, 0, None) == 1
-    assert lib.topk_transform_window(one, 8, one, one, 1, 0, one, None, 0, None) == 2
+    assert lib.topk_transform_window(one, 8, None, one, 0, 1, 16, one, None, 0, None) == 1
+    assert lib.topk_transform_window(one, 0, one, one, 0, 1, 16, one, None, 0, None) == 1
+    assert lib.topk_transform_window(one, 8, one, one, -1, 1, 16, one, None, 0, None) == 1
+    assert lib.topk_transform_window(one, 8, one, one, 0, 1, 0, one, None, 0, None) == 2
 
 
 def test_grouped_layout_and_host_checks(lib):
@@ -96,6 +97,13 @@ def test_grouped_layout_and_host_checks(lib):
                            out=one)) == 1                                 # window without starts
     assert group(P(form=0, batch=1, k=4, row_stride=8, scores=18, seq_lens=one,
                    out=one)) == 1                                         # misaligned scores
+
+
+def test_cta_threads_control_round_trip(lib):
+    prev = lib.topk_set_cta_threads(256)
+    assert lib.topk_set_cta_threads(512) == 256
+    assert lib.topk_set_cta_threads(7) == 512     # anything else: automatic
+    assert lib.topk_set_cta_threads(prev) == 0
 
 
 def test_tuning_controls_round_trip(lib):

@@ -31,13 +31,16 @@ def pkg():
 
 
 @contextlib.contextmanager
-def settings(pkg, split=None, tie_cap=None, fast=None):
+def settings(pkg, split=None, tie_cap=None, fast=None, cta=None):
     prev_split = pkg.topk_set_row_split(split) if split is not None else None
     prev_cap = pkg.topk_set_tie_capacity(tie_cap) if tie_cap is not None else None
     prev_fast = pkg.topk_set_fast_tier(fast) if fast is not None else None
+    prev_cta = pkg.topk_set_cta_threads(cta) if cta is not None else None
     try:
         yield
     finally:
+        if cta is not None:
+            pkg.topk_set_cta_threads(prev_cta)
         if split is not None:
             pkg.topk_set_row_split(prev_split)
         if tie_cap is not None:
@@ -58,7 +61,10 @@ def run_gpu(pkg, w, stream=None) -> np.ndarray:
         pkg.topk_transform_paged(scores, seq, pt, w.page_size, w.k, out=out, stream=stream)
     elif w.form == "window":
         st = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
-        pkg.topk_transform_window(scores, st, seq, w.k, out=out, stream=stream)
+        # the window-length hint on the prefill workloads, none (the row length) on the rest
+        hint = w.max_row_len if w.name.startswith("window_b") else 0
+        pkg.topk_transform_window(scores, st, seq, w.k, max_row_len_hint=hint, out=out,
+                                  stream=stream)
     else:
         rs = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
         hint = int(np.max(w.seq_lens, initial=0))
@@ -399,6 +405,7 @@ def problem_of(w, dev):
         q["max_row_len_hint"] = int(np.max(w.seq_lens, initial=0))
     elif w.form == "window":
         q["starts"] = torch.from_numpy(np.ascontiguousarray(w.row_starts)).to(dev)
+        q["max_row_len_hint"] = w.max_row_len
     return q
 
 
@@ -461,3 +468,111 @@ def test_grouped_equals_single_calls(pkg):
     w = workloads.config3(128)
     (got,) = run_grouped(pkg, [w])
     assert same_sets(got, run_gpu(pkg, w)).all()
+
+
+# ------------------------------------------------------------ many rows (the 256-thread build)
+# Launches of more rows than two 512-thread CTAs per SM hold (304 on 152 SMs) with
+# k <= 1024 run the kernels built with 256-thread CTAs.
+
+def many_rows(form, batch, stride, k, seed, dist="normal"):
+    g = np.random.Generator(np.random.PCG64(seed))
+    scores = workloads.random_rows(g, batch, stride, dist, dup=True)
+    seq = g.integers(0, stride + 20, size=batch).astype(np.int32)
+    seq[: batch // 2] = stride  # half the rows full length (sampled filter)
+    if form == "raw":
+        return workloads.Workload(f"many_raw_{batch}_{stride}", "raw", k, scores, seq)
+    if form == "paged":
+        pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, 64))
+        return workloads.Workload(f"many_paged_{batch}_{stride}", "paged", k, scores, seq, pt, 64)
+    lens = np.minimum(seq, stride).astype(np.int64)
+    starts = np.concatenate([[1], 1 + np.cumsum(lens + 3)[:-1]]).astype(np.int32)
+    packed = np.zeros(int(starts[-1] + lens[-1] + 5), np.float32)
+    for b in range(batch):
+        packed[starts[b]:starts[b] + lens[b]] = scores[b, :lens[b]]
+    return workloads.Workload(f"many_ragged_{batch}_{stride}", "ragged", k, packed,
+                              lens.astype(np.int32), None, 64, starts)
+
+
+@pytest.mark.parametrize("form", ["raw", "paged", "ragged"])
+@pytest.mark.parametrize("fast", [1, 0])
+def test_many_rows(pkg, form, fast):
+    w = many_rows(form, 400, 8192, 1024, 41 + fast, "banded" if fast else "normal")
+    with settings(pkg, fast=fast):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+def test_many_long_paged_rows(pkg):
+    """Rows of more pages than the 256-thread build stages (1024): the page table is
+    read from global memory."""
+    w = many_rows("paged", 320, 70000, 1024, 43)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+@pytest.mark.parametrize("tie_cap", [0, 64, 4096])
+def test_many_rows_tie_capacity(pkg, tie_cap):
+    w = many_rows("raw", 320, 6000, 700, 47 + tie_cap, "narrow")
+    with settings(pkg, tie_cap=tie_cap):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("k", [1, 1024, 1025])
+def test_many_rows_k_switches_build(pkg, k):
+    w = many_rows("raw", 330, 5000, k, 53)
+    assert_parity(w, run_gpu(pkg, w))
+
+
+def test_grouped_many_rows(pkg):
+    ws = [many_rows("raw", 40, 4096 + 512 * i, 1024, 60 + i) for i in range(12)]
+    for w, got in zip(ws, run_grouped(pkg, ws)):
+        assert_parity(w, got)
+
+
+# ------------------------------------------------------------ the 256-thread build on every path
+
+@pytest.mark.parametrize("fast", [True, False])
+@pytest.mark.parametrize("split", [1, 4, 16])
+@pytest.mark.parametrize("dist", ["normal", "decode", "banded", "narrow", "subnormal", "heavy_tail"])
+def test_every_row_split_cta256(pkg, split, dist, fast):
+    w = _mixed(100 + split, dist)
+    with settings(pkg, split=split, fast=fast, cta=256):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("tie_cap", [0, 16, 300, 3072, 4096])
+@pytest.mark.parametrize("split", [1, 4])
+@pytest.mark.parametrize("dist", ["decode", "banded", "narrow", "subnormal"])
+def test_tie_buffer_capacity_cta256(pkg, tie_cap, split, dist):
+    w = _mixed(200 + tie_cap, dist, k=2048)
+    with settings(pkg, split=split, tie_cap=tie_cap, cta=256):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+def pages_workloads():
+    return [workloads.config1(), workloads.config2(8192), workloads.config2(32768),
+            workloads.config3(64), workloads.config3(256, "raw"), workloads.config4("banded"),
+            workloads.config5(1), workloads.prefill_windows(256, 8192, window=2000)]
+
+
+@pytest.mark.parametrize("cta", [256, 512])
+def test_pages_workloads_on_each_build(pkg, cta):
+    for w in pages_workloads():
+        with settings(pkg, cta=cta):
+            got = run_gpu(pkg, w)
+        assert_parity(w, got, check_rows=8)
+
+
+@pytest.mark.parametrize("split", [1, 16])
+def test_all_equal_rows_cta256(pkg, split):
+    batch, stride, k = 3, 50000, 2048
+    scores = np.full((batch, stride), 1.5, np.float32)
+    scores[1, ::7] = -0.0
+    scores[2] = 0.0
+    seq = np.array([stride, stride - 3, 40001], np.int32)
+    w = workloads.Workload("all_equal_cta256", "raw", k, scores, seq)
+    with settings(pkg, split=split, cta=256):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)

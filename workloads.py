@@ -158,6 +158,20 @@ class Workload:
             return int(np.maximum(hi - lo, 0).sum())
         return int(np.clip(self.seq_lens, 0, cap).sum())
 
+    @property
+    def max_row_len(self) -> int:
+        """The longest valid row (window) length, e.g. for a length hint."""
+        if self.batch == 0:
+            return 0
+        if self.form == "ragged":
+            return int(np.maximum(self.seq_lens, 0).max())
+        cap = self.scores.shape[1]
+        hi = np.clip(self.seq_lens.astype(np.int64), 0, cap)
+        if self.form == "window":
+            lo = np.clip(self.row_starts.astype(np.int64), 0, cap)
+            return int(np.maximum(hi - lo, 0).max())
+        return int(hi.max())
+
     def as_raw(self) -> "Workload":
         return dataclasses.replace(self, form="raw", page_table=None)
 
