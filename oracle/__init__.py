@@ -78,6 +78,10 @@ class Oracle:
         lib.oracle_topk_ragged.restype = ctypes.c_int
         lib.oracle_topk_ragged.argtypes = [f32p, i32p, i32p, ctypes.c_int32,
                                            ctypes.c_int32, i32p, ctypes.c_int]
+        lib.oracle_topk_values.restype = ctypes.c_int
+        lib.oracle_topk_values.argtypes = [ctypes.c_int32, f32p, ctypes.c_int64, i32p, i32p, i32p,
+                                           ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32, i32p, f32p, ctypes.c_int]
         lib.oracle_topk_window.restype = ctypes.c_int
         lib.oracle_topk_window.argtypes = [f32p, ctypes.c_int64, i32p, i32p, ctypes.c_int32,
                                            ctypes.c_int32, i32p, ctypes.c_int]
@@ -160,6 +164,30 @@ class Oracle:
             raise ValueError(f"oracle_topk_window: invalid arguments (status {rc})")
         return out
 
+    def run_values(self, w, threads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+        """Run one ``workloads.Workload`` with the values output: (positions in rank
+        order, fp32 values, -inf in the padding slots)."""
+        forms = {"raw": 0, "paged": 1, "ragged": 2, "window": 3}
+        s, sp = _f32(w.scores)
+        B, k = w.batch, w.k
+        L, lp = _i32(w.seq_lens)
+        rs, rsp = _i32(w.row_starts if w.row_starts is not None else np.zeros(B, np.int32))
+        pt, ptp = _i32(w.page_table if w.page_table is not None else np.zeros((B, 1), np.int32))
+        if w.form == "ragged" and B and (rs.astype(np.int64) + np.maximum(L, 0)).max() > s.size:
+            raise ValueError("a ragged row runs outside the packed scores buffer")
+        if w.form == "paged" and pt.shape[1] * w.page_size < min(s.shape[1], max(int(L.max(initial=0)), 0)):
+            raise ValueError("page_table does not cover the rows")
+        out = np.empty((B, k), dtype=np.int32)
+        vals = np.empty((B, k), dtype=np.float32)
+        _, op = _i32(out)
+        _, vp = _f32(vals)
+        stride = s.shape[1] if s.ndim == 2 else 0
+        rc = self.lib.oracle_topk_values(forms[w.form], sp, stride, rsp, lp, ptp, pt.shape[1],
+                                         w.page_size, B, k, op, vp, threads)
+        if rc != 0:
+            raise ValueError(f"oracle_topk_values: invalid arguments (status {rc})")
+        return out, vals
+
     def run(self, w, threads: int = 0) -> np.ndarray:
         """Run one ``workloads.Workload``."""
         if w.form == "raw":
@@ -204,6 +232,10 @@ def topk_ragged(scores, row_starts, seq_lens, k: int, threads: int = 0) -> np.nd
 
 def topk_window(scores, starts, seq_lens, k: int, threads: int = 0) -> np.ndarray:
     return default().topk_window(scores, starts, seq_lens, k, threads)
+
+
+def run_values(w, threads: int = 0):
+    return default().run_values(w, threads)
 
 
 def run(w, threads: int = 0) -> np.ndarray:

@@ -43,12 +43,20 @@
 //   row, emitting row columns, is the reading adopted.)
 //   5. Slots m .. k-1 get -1 ([36004] "关键源码片段": the test pre-fills the
 //      output with -1, so short rows leave -1 behind).
+//   The m positions are written in rank order: largest key first, equal keys by
+//   smaller position first (the order of the stable sort). This is the order of the
+//   optional sorted output; the plain output may hold the same set in any order.
+//   Optionally, values[b][i] gets the fp32 score of the element in slot i (its bit
+//   pattern unchanged) and -inf in the padding slots (the extra outputs of the
+//   "runtime k generalisation" item of the next steps; the pages name returned
+//   values without fixing the padding, -inf is the reading adopted).
 //
 // Build: g++ -O2 -std=c++17 -shared -fPIC -pthread topk_oracle.cpp
 
 #include <sched.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <thread>
@@ -94,6 +102,7 @@ struct Job {
   int32_t page_size;           // paged
   int32_t k;
   int32_t* out;                // [batch, k]
+  float* values;               // [batch, k] or null
 };
 
 void run_row(const Job& job, int64_t b, std::vector<int32_t>& chosen) {
@@ -130,6 +139,11 @@ void run_row(const Job& job, int64_t b, std::vector<int32_t>& chosen) {
     out[i] = v;
   }
   for (int64_t i = m; i < job.k; ++i) out[i] = -1;
+  if (job.values != nullptr) {
+    float* v = job.values + b * static_cast<int64_t>(job.k);
+    for (int64_t i = 0; i < m; ++i) v[i] = row[chosen[i]];
+    for (int64_t i = m; i < job.k; ++i) v[i] = -INFINITY;
+  }
 }
 
 int usable_cores() {
@@ -185,7 +199,7 @@ int oracle_usable_cores(void) { return usable_cores(); }
 // threads < 1 means every usable core. Returns 0, or 1 on invalid arguments.
 int oracle_topk_raw(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                     int32_t batch, int32_t k, int32_t* out, int threads) {
-  Job job{kRaw, scores, row_stride, nullptr, seq_lens, nullptr, 0, 0, k, out};
+  Job job{kRaw, scores, row_stride, nullptr, seq_lens, nullptr, 0, 0, k, out, nullptr};
   return run(job, batch, threads);
 }
 
@@ -195,7 +209,7 @@ int oracle_topk_paged(const float* scores, int64_t row_stride, const int32_t* se
                       int32_t page_size, int32_t batch, int32_t k, int32_t* out,
                       int threads) {
   Job job{kPaged, scores, row_stride, nullptr, seq_lens, page_table, page_table_stride,
-          page_size, k, out};
+          page_size, k, out, nullptr};
   return run(job, batch, threads);
 }
 
@@ -203,7 +217,7 @@ int oracle_topk_paged(const float* scores, int64_t row_stride, const int32_t* se
 int oracle_topk_ragged(const float* scores, const int32_t* row_starts,
                        const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
                        int threads) {
-  Job job{kRagged, scores, 0, row_starts, seq_lens, nullptr, 0, 0, k, out};
+  Job job{kRagged, scores, 0, row_starts, seq_lens, nullptr, 0, 0, k, out, nullptr};
   return run(job, batch, threads);
 }
 
@@ -212,7 +226,20 @@ int oracle_topk_ragged(const float* scores, const int32_t* row_starts,
 int oracle_topk_window(const float* scores, int64_t row_stride, const int32_t* starts,
                        const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out,
                        int threads) {
-  Job job{kWindow, scores, row_stride, starts, seq_lens, nullptr, 0, 0, k, out};
+  Job job{kWindow, scores, row_stride, starts, seq_lens, nullptr, 0, 0, k, out, nullptr};
+  return run(job, batch, threads);
+}
+
+// Any form (0 raw, 1 paged, 2 ragged, 3 window; the arguments a form does not use
+// are ignored) with the optional values output (null: not written). Positions are
+// in rank order.
+int oracle_topk_values(int32_t form, const float* scores, int64_t row_stride,
+                       const int32_t* row_starts, const int32_t* seq_lens,
+                       const int32_t* page_table, int64_t page_table_stride, int32_t page_size,
+                       int32_t batch, int32_t k, int32_t* out, float* values, int threads) {
+  if (form < kRaw || form > kWindow) return 1;
+  Job job{static_cast<Form>(form), scores, row_stride, row_starts, seq_lens, page_table,
+          page_table_stride, page_size, k, out, values};
   return run(job, batch, threads);
 }
 

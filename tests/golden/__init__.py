@@ -29,6 +29,8 @@ class Case:
     page_size: int = 64
     page_table: np.ndarray | None = None
     row_starts: np.ndarray | None = None
+    expect_sorted: np.ndarray | None = None
+    expect_values: np.ndarray | None = None
 
 
 def load_cases(filename: str = "topk_cases.txt") -> list[Case]:
@@ -78,6 +80,12 @@ def load_cases(filename: str = "topk_cases.txt") -> list[Case]:
         if "page_table" in fields:
             case.page_table = np.array([[int(t) for t in r] for r in rows("page_table")],
                                        dtype=np.int32)
+        if "expect_sorted" in fields:
+            case.expect_sorted = np.array([[int(t) for t in r] for r in rows("expect_sorted")],
+                                          dtype=np.int32)
+        if "expect_values" in fields:
+            case.expect_values = np.array([[_value(t) for t in r] for r in rows("expect_values")],
+                                          dtype=np.float32)
         if "row_starts" in fields:
             case.row_starts = np.array([int(t) for t in fields["row_starts"][0].split()],
                                        dtype=np.int32)

@@ -58,6 +58,15 @@ def pin_golden(o):
         exp = np.sort(c.expect, axis=1)
         assert got.shape == exp.shape and (got == exp).all(), (
             f"golden case {c.name}: got {got.tolist()}, expected {exp.tolist()}")
+        if c.expect_sorted is None:
+            continue
+        w = workloads.Workload(c.name, c.form, c.k, c.scores, c.seq_lens, c.page_table,
+                               c.page_size, c.row_starts)
+        pos, vals = o.run_values(w, 1)
+        assert (pos == c.expect_sorted).all(), (
+            f"golden case {c.name}: rank order {pos.tolist()}, expected {c.expect_sorted.tolist()}")
+        assert (vals.view(np.uint32) == c.expect_values.view(np.uint32)).all(), (
+            f"golden case {c.name}: values {vals.tolist()}, expected {c.expect_values.tolist()}")
 
 
 def _value_order(x: float):
@@ -107,6 +116,16 @@ def pin_brute_force(o, trials: int = 1500, seed: int = 7):
         got = set(int(v) for v in out if v >= 0)
         assert got == exp and int((out == -1).sum()) == k - len(exp), (
             f"trial {t}: row {row.tolist()} k={k}: oracle {out.tolist()}, brute force {sorted(exp)}")
+        # rank order: larger value first, equal values by smaller position first,
+        # then the padding; values are the selected scores, -inf pads
+        ranked = sorted(exp, key=lambda i: (tuple(-x for x in _value_order(row[i])), i))
+        assert out.tolist() == ranked + [-1] * (k - len(exp)), (
+            f"trial {t}: row {row.tolist()} k={k}: oracle order {out.tolist()}, expected {ranked}")
+        w = workloads.Workload("bf", "raw", k, row[None, :], np.array([L], np.int32))
+        pos, vals = o.run_values(w, 1)
+        want = np.array([row[i] for i in ranked] + [-np.inf] * (k - len(exp)), np.float32)
+        assert (pos[0] == out).all() and (vals[0].view(np.uint32) == want.view(np.uint32)).all(), (
+            f"trial {t}: values {vals[0].tolist()}, expected {want.tolist()}")
 
 
 def pin_brute_force_window(o, trials: int = 600, seed: int = 29):

@@ -42,6 +42,12 @@ MUTANTS = [
      "lo = std::min<int64_t>(job.row_starts[b], job.row_stride);"),
     ("window_row_not_offset", "row = job.scores + b * job.row_stride + lo;",
      "row = job.scores + b * job.row_stride;"),
+    ("rank_order_reversed", "for (int64_t i = 0; i < m; ++i) chosen[i] = pairs[i].pos;",
+     "for (int64_t i = 0; i < m; ++i) chosen[i] = pairs[m - 1 - i].pos;"),
+    ("values_from_first_slot", "for (int64_t i = 0; i < m; ++i) v[i] = row[chosen[i]];",
+     "for (int64_t i = 0; i < m; ++i) v[i] = row[chosen[0]];"),
+    ("values_padding_zero", "for (int64_t i = m; i < job.k; ++i) v[i] = -INFINITY;",
+     "for (int64_t i = m; i < job.k; ++i) v[i] = 0.0f;"),
 ]
 
 
