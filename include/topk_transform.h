@@ -140,10 +140,20 @@ typedef enum {
   TOPK_FORM_WINDOW = 3
 } topk_form_t;
 
+/* Options of a problem (topk_problem_t.flags). TOPK_FLAG_SORTED: the m selected
+ * slots of each row in rank order (largest score first, equal scores by smaller
+ * position first; the -1 padding after them). Needs a device workspace of
+ * topk_problem_workspace_bytes bytes; the ordering runs as a second kernel per
+ * sorted problem. (The "extra outputs" of the next steps after the pages' design:
+ * the pages fix the set, not an order.) */
+#define TOPK_FLAG_SORTED 1u
+
 /* One problem: the arguments of its form's entry point. Fields a form does not
  * use are ignored (row_stride: raw, paged, window; page_table, page_table_stride,
  * page_size: paged; row_starts: ragged row offsets or window starts;
- * max_row_len_hint: ragged and window, as for their entry points). */
+ * max_row_len_hint: ragged and window, as for their entry points).
+ * values (optional, [batch, k] fp32, device): each slot's score (its fp32 bits
+ * unchanged), -inf in the padding slots; NULL: not written. */
 typedef struct {
   int32_t form;               /* topk_form_t */
   int32_t batch;              /* rows, >= 0 (0: nothing to do) */
@@ -157,6 +167,9 @@ typedef struct {
   const int32_t* row_starts;
   const int32_t* page_table;
   int32_t* out;               /* [batch, k] */
+  float* values;              /* [batch, k] or NULL */
+  uint32_t flags;             /* TOPK_FLAG_* */
+  uint32_t reserved;          /* 0 */
 } topk_problem_t;
 
 /* Most problems one grouped call takes. */
@@ -166,10 +179,19 @@ typedef struct {
  * copy of the layout). */
 size_t topk_problem_bytes(void);
 
+/* Device workspace bytes a grouped call with these problems needs: for each
+ * problem with TOPK_FLAG_SORTED, 8 bytes per output slot (batch * k), rounded up
+ * to 256 bytes; 0 when no problem asks for sorted output. problems: host array of
+ * n_problems (invalid arguments give 0). */
+size_t topk_problem_workspace_bytes(const topk_problem_t* problems, int32_t n_problems);
+
 /* problems: HOST array of n_problems (0 .. TOPK_MAX_GROUP) descriptors, read
  * during the call only; the pointers inside are device memory, as for the single
  * entry points. Every problem is checked first, in order: on the first problem
- * that fails its check nothing is launched and its status is returned.
+ * that fails its check nothing is launched and its status is returned; a
+ * workspace smaller than topk_problem_workspace_bytes returns
+ * TOPK_ERR_WORKSPACE_TOO_SMALL, also before any launch (workspace: device memory,
+ * 256-byte aligned, owned by the caller, used until the launches finish).
  * Problems of one form share a launch; distinct output buffers are required. */
 int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -26,7 +26,8 @@ from . import build as _build
 __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
     "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged", "topk_transform_window",
-    "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "topk_set_cta_threads",
+    "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "TOPK_FLAG_SORTED",
+    "topk_set_cta_threads",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
@@ -74,6 +75,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_transform_grouped.argtypes = [vp, i32, vp, sz, vp]
             lib.topk_problem_bytes.restype = sz
             lib.topk_problem_bytes.argtypes = []
+            lib.topk_problem_workspace_bytes.restype = sz
+            lib.topk_problem_workspace_bytes.argtypes = [vp, i32]
             if lib.topk_problem_bytes() != ctypes.sizeof(TopkProblem):
                 raise RuntimeError("topk_problem_t layout differs between the library and "
                                    "this binding")
@@ -240,7 +243,11 @@ class TopkProblem(ctypes.Structure):
                 ("page_table_stride", ctypes.c_int64), ("max_row_len_hint", ctypes.c_int64),
                 ("scores", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
                 ("row_starts", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
-                ("out", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("values", ctypes.c_void_p), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+TOPK_FLAG_SORTED = 1
 
 
 def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tensor]:
@@ -249,7 +256,11 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
     Each problem is a dict with "form" ("raw", "paged", "ragged" or "window"), "k",
     "scores", "seq_lens" and what its form needs: "page_table" and "page_size"
     (paged), "row_starts" and optionally "max_row_len_hint" (ragged), "starts" and
-    optionally "max_row_len_hint" (window); "out" is optional. Returns the output tensors, in order."""
+    optionally "max_row_len_hint" (window); "out" is optional. Options: "values", a
+    [batch, k] fp32 device tensor that receives each slot's score (-inf in the
+    padding slots), and "sorted": True for the slots in rank order (largest score
+    first, equal scores by smaller position first). Sorted problems use a device
+    workspace this function allocates. Returns the output tensors, in order."""
     lib = load_library()
     if len(problems) > TOPK_MAX_GROUP:
         raise ValueError(f"at most {TOPK_MAX_GROUP} problems per grouped call")
@@ -295,14 +306,26 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
             arr[i].row_starts = q["starts"].data_ptr()
             arr[i].max_row_len_hint = int(q.get("max_row_len_hint", 0))
         out = _out(q.get("out"), batch, k, d)
+        vals = q.get("values")
+        if vals is not None:
+            _cuda_tensor(vals, "values", torch.float32, d)
+            if tuple(vals.shape) != (batch, k) or not vals.is_contiguous():
+                raise ValueError(f"values must be a contiguous fp32 tensor of shape ({batch}, {k})")
+            arr[i].values = vals.data_ptr()
+        arr[i].flags = TOPK_FLAG_SORTED if q.get("sorted", False) else 0
         arr[i].form, arr[i].batch, arr[i].k = _FORMS[form], batch, k
         arr[i].scores, arr[i].seq_lens, arr[i].out = scores.data_ptr(), q["seq_lens"].data_ptr(), out.data_ptr()
         outs.append(out)
     if not problems:
         return outs
+    ws_bytes = int(lib.topk_problem_workspace_bytes(ctypes.addressof(arr), len(problems)))
     with torch.cuda.device(dev):
-        st = lib.topk_transform_grouped(ctypes.addressof(arr), len(problems), None, 0,
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+        st = lib.topk_transform_grouped(ctypes.addressof(arr), len(problems),
+                                        ws.data_ptr() if ws is not None else None, ws_bytes,
                                         _stream(stream, dev))
+        if ws is not None:  # the launches on `stream` read it until they finish
+            ws.record_stream(torch.cuda.current_stream(dev) if stream is None else stream)
     _check(st, "topk_transform_grouped")
     return outs
 

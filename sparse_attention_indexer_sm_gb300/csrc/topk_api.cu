@@ -113,6 +113,7 @@ int build_params(const topk_problem_t& q, Params* p, int64_t* len_hint) {
   if (q.batch < 0) return TOPK_ERR_INVALID_ARGUMENT;
   if (q.k < 1 || q.k > TOPK_MAX_K) return TOPK_ERR_UNSUPPORTED_K;
   if (q.form < TOPK_FORM_RAW || q.form > TOPK_FORM_WINDOW) return TOPK_ERR_INVALID_ARGUMENT;
+  if ((q.flags & ~TOPK_FLAG_SORTED) != 0u || q.reserved != 0u) return TOPK_ERR_INVALID_ARGUMENT;
   *p = Params{};
   p->batch = q.batch;
   p->k = q.k;
@@ -125,6 +126,7 @@ int build_params(const topk_problem_t& q, Params* p, int64_t* len_hint) {
   p->scores = q.scores;
   p->seq_lens = q.seq_lens;
   p->out = q.out;
+  p->values = q.values;
   if (q.form == TOPK_FORM_RAGGED) {
     if (q.row_starts == nullptr || q.max_row_len_hint < 0) return TOPK_ERR_INVALID_ARGUMENT;
     p->row_starts = q.row_starts;
@@ -185,6 +187,20 @@ int run_one(const topk_problem_t& q, cudaStream_t stream) {
   return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
 }
 
+// Bytes of the sorted problems' staging areas (each batch * k pairs of 8 bytes,
+// rounded up to 256); offsets[i] (if given) gets problem i's offset.
+size_t staging_bytes(const topk_problem_t* problems, int32_t n, size_t* offsets) {
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (offsets != nullptr) offsets[i] = total;
+    const topk_problem_t& q = problems[i];
+    if ((q.flags & TOPK_FLAG_SORTED) == 0u || q.batch <= 0 || q.k <= 0) continue;
+    const size_t bytes = static_cast<size_t>(q.batch) * static_cast<size_t>(q.k) * 8u;
+    total += (bytes + 255u) / 256u * 256u;
+  }
+  return total;
+}
+
 topk_problem_t problem(int32_t form, const float* scores, int64_t row_stride,
                        const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out) {
   topk_problem_t q = {};
@@ -207,6 +223,11 @@ size_t topk_workspace_bytes(int32_t /*batch*/, int64_t /*max_row_len*/, int32_t 
 }
 
 size_t topk_problem_bytes(void) { return sizeof(topk_problem_t); }
+
+size_t topk_problem_workspace_bytes(const topk_problem_t* problems, int32_t n_problems) {
+  if (problems == nullptr || n_problems < 0 || n_problems > TOPK_MAX_GROUP) return 0;
+  return staging_bytes(problems, n_problems, nullptr);
+}
 
 int topk_transform_raw(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                        int32_t batch, int32_t k, int32_t* out, void* /*workspace*/,
@@ -246,8 +267,7 @@ int topk_transform_window(const float* scores, int64_t row_stride, const int32_t
 }
 
 int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
-                           void* /*workspace*/, size_t /*workspace_bytes*/,
-                           cudaStream_t stream) {
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
   if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
   // every problem is checked before anything is launched
@@ -260,6 +280,17 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     const int st = build_params(problems[i], &params[i], &hints[i]);
     if (st != TOPK_OK) return st;
     rows_of_form[problems[i].form] += problems[i].batch;
+  }
+  // sorted problems stage (key, position) pairs in the workspace
+  size_t offsets[TOPK_MAX_GROUP];
+  const size_t need = staging_bytes(problems, n_problems, offsets);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return workspace_bytes < need ? TOPK_ERR_WORKSPACE_TOO_SMALL : TOPK_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < n_problems; ++i)
+      if ((problems[i].flags & TOPK_FLAG_SORTED) != 0u && problems[i].batch > 0)
+        params[i].staged = reinterpret_cast<uint2*>(static_cast<char*>(workspace) + offsets[i]);
   }
   DeviceState* ds = nullptr;
   bool any = false;
@@ -287,15 +318,26 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     if (rows * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
     gp.row_begin[gp.n] = static_cast<int32_t>(rows);
     int32_t k_max = 0;
-    for (int i = 0; i < gp.n; ++i) k_max = std::max(k_max, gp.probs[i].k);
+    bool opts = false;  // the values output or the sorted option
+    for (int i = 0; i < gp.n; ++i) {
+      k_max = std::max(k_max, gp.probs[i].k);
+      opts = opts || gp.probs[i].values != nullptr || gp.probs[i].staged != nullptr;
+    }
     cudaError_t e;
     if (use_cta256(rows, hint, g, k_max, ds->sm_count)) {
       for (int i = 0; i < gp.n; ++i)
         gp.probs[i].tie_cap = std::min(gp.probs[i].tie_cap, topk_gb300::kTieCap256);
-      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, stream);
+      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts, stream);
     } else {
-      e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, stream);
+      e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, opts, stream);
     }
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  for (int i = 0; i < n_problems; ++i) {  // the sort pass of each sorted problem
+    if (params[i].staged == nullptr) continue;
+    apply_settings(knobs, &params[i]);
+    const cudaError_t e =
+        topk_gb300::cta512::sort_rows(static_cast<Form>(problems[i].form), params[i], stream);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return TOPK_OK;

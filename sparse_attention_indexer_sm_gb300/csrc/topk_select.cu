@@ -544,11 +544,24 @@ struct OutMap {
   int32_t ps;             // page size
   int32_t ps_shift;       // log2(ps) or -1
   int32_t rstart;         // ragged: row start in the packed buffer; window: its first column
+  float* values;          // this row's values output, or null
+  uint2* staged;          // this row's (key, position) staging for the sort pass, or null
 };
+
+// The kernels' template argument F is a Form, plus kOpts when the launch has the
+// values output or the sorted option (so that launches without them carry neither).
+constexpr int kOpts = 4;
+__host__ __device__ constexpr int form_of(int F) { return F & 3; }
+__host__ __device__ constexpr bool opts_of(int F) { return (F & kOpts) != 0; }
+
+// The fp32 bit pattern of an order-preserving key (the inverse of order_key).
+__device__ __forceinline__ uint32_t key_bits(uint32_t key) {
+  return (key & 0x80000000u) != 0u ? key ^ 0x80000000u : ~key;
+}
 
 template <int F>
 __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
-  if constexpr (F == kPaged) {
+  if constexpr (form_of(F) == kPaged) {
     int32_t page, off;
     if (m.ps_shift >= 0) {
       page = j >> m.ps_shift;
@@ -559,20 +572,43 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
     }
     const int32_t phys = m.pt_smem != nullptr ? m.pt_smem[page] : __ldg(m.pt_row + page);
     return phys * m.ps + off;
-  } else if constexpr (F == kRagged || F == kWindow) {
+  } else if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) {
     return m.rstart + j;
   } else {
     return j;
   }
 }
 
-// Every write of a row's output goes through here: slots at or beyond k are
-// dropped. By construction no slot is ever >= k; the check keeps a miscount (say,
-// scores modified while the kernel runs) from writing outside the row.
+// Every write of a row's output goes through here: position j with key `key` in
+// slot `slot`, mapped, and its value when asked for; or, for the sorted output,
+// the pair (key, j) to the staging buffer the sort pass orders. Slots at or beyond
+// k are dropped. By construction no slot is ever >= k; the check keeps a miscount
+// (say, scores modified while the kernel runs) from writing outside the row.
 template <int F>
 __device__ __forceinline__ void emit(int32_t* out, int32_t k, uint32_t slot, const OutMap& m,
-                                     int32_t j) {
-  if (slot < static_cast<uint32_t>(k)) out[slot] = map_pos<F>(m, j);
+                                     int32_t j, uint32_t key) {
+  if (slot >= static_cast<uint32_t>(k)) return;
+  if constexpr (opts_of(F)) {
+    if (m.staged != nullptr) {
+      m.staged[slot] = make_uint2(key, static_cast<uint32_t>(j));
+      return;
+    }
+    if (m.values != nullptr) m.values[slot] = __uint_as_float(key_bits(key));
+  }
+  out[slot] = map_pos<F>(m, j);
+}
+
+// An empty slot: -1 (and -inf for the value), or the padding pair of the staging.
+template <int F>
+__device__ __forceinline__ void emit_pad(int32_t* out, uint32_t slot, const OutMap& m) {
+  if constexpr (opts_of(F)) {
+    if (m.staged != nullptr) {
+      m.staged[slot] = make_uint2(0u, 0xFFFFFFFFu);
+      return;
+    }
+    if (m.values != nullptr) m.values[slot] = __uint_as_float(0xFF800000u);  // -inf
+  }
+  out[slot] = -1;
 }
 
 // ------------------------------------------------------------------ fast tier
@@ -1006,7 +1042,7 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
       sel = hi_bits(compose(e), p) >= P;
     }
     const uint32_t slot = warp_reserve_bit(&ctl.out_cnt, sel);
-    if (sel && slot < want) emit<F>(out, k, k_above + slot, m, static_cast<int32_t>(e.y));
+    if (sel && slot < want) emit<F>(out, k, k_above + slot, m, static_cast<int32_t>(e.y), e.x);
   }
 }
 
@@ -1055,7 +1091,10 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
     const uint32_t c = (cls >> (2 * r)) & 3u;
     const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
     if (c == 1u) {
-      if (ws < above) emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(buf[i].y));
+      if (ws < above) {
+        const uint2 e = buf[i];
+        emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y), e.x);
+      }
       ++ws;
     } else if (c == 2u) {
       if (ts < ct) list[ts] = buf[i];
@@ -1075,7 +1114,7 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
         const uint64_t w = (static_cast<uint64_t>(o.x) << 32) | static_cast<uint64_t>(~o.y);
         r += w > v ? 1u : 0u;
       }
-      if (r < need) emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y));
+      if (r < need) emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y), e.x);
     }
     return;
   }
@@ -1108,7 +1147,7 @@ __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, in
     const bool tie = ok && (key >> shift) == prefix;
     const uint32_t ws = warp_reserve_bit(&ctl.win_cnt, win);
     const uint32_t ts = warp_reserve_bit(&ctl.tie_cnt, tie);
-    if (win) emit<F>(out, k, win_base + ws, m, j);
+    if (win) emit<F>(out, k, win_base + ws, m, j, key);
     if (tie) put_tie(tie_base + ts, key, j);
   }
   for (int32_t base = 0; base < s.nq; base += kUnroll * kThreads) {
@@ -1143,7 +1182,7 @@ __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, in
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int bit = 4 * u + c;
-          if ((wb >> bit) & 1u) emit<F>(out, k, win_base + ws++, m, j + c);
+          if ((wb >> bit) & 1u) emit<F>(out, k, win_base + ws++, m, j + c, key[bit]);
           if ((tb >> bit) & 1u) put_tie(tie_base + ts++, key[bit], j + c);
         }
       }
@@ -1174,13 +1213,13 @@ __device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t
     uint32_t ws = warp_reserve(&ctl.win_cnt, 0u, false, __popc(wb));
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if ((wb >> u) & 1u) emit<F>(out, k, win_base + ws++, m, j0 + u);
+      if ((wb >> u) & 1u) emit<F>(out, k, win_base + ws++, m, j0 + u, key[u]);
     uint32_t total;
     uint32_t r = taken + block_excl_scan(__popc(eb), ctl, &total);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if ((eb >> u) & 1u) {
-        if (r < quota) emit<F>(out, k, eq_slot0 + r, m, j0 + u);
+        if (r < quota) emit<F>(out, k, eq_slot0 + r, m, j0 + u, tau);
         ++r;
       }
     }
@@ -1209,13 +1248,13 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // the row's length (and start) first: everything waits for them
   const int32_t seq = p.seq_lens[row];
   int32_t start = 0;  // ragged: row offset; window: window start
-  if constexpr (F == kRagged || F == kWindow) start = p.row_starts[row];
+  if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) start = p.row_starts[row];
   // raw, paged: the row's start does not depend on its length, so the sample is
   // loaded (over the whole row stride; elements at or past the length are ignored
   // later) while the length is still on its way
   Sample sm;
   bool sample_loaded = false;
-  if constexpr (F == kRaw || F == kPaged) {
+  if constexpr (form_of(F) == kRaw || form_of(F) == kPaged) {
     if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
       load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
                              static_cast<int32_t>(p.row_stride), rank, G),
@@ -1246,13 +1285,17 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   m.ps = p.page_size;
   m.ps_shift = p.page_shift;
   m.rstart = 0;
+  m.values = opts_of(F) && p.values != nullptr ? p.values + static_cast<int64_t>(row) * p.k
+                                               : nullptr;
+  m.staged = opts_of(F) && p.staged != nullptr ? p.staged + static_cast<int64_t>(row) * p.k
+                                               : nullptr;
   const float* rowp;
   int32_t L;
-  if constexpr (F == kRagged) {
+  if constexpr (form_of(F) == kRagged) {
     m.rstart = start;
     rowp = p.scores + m.rstart;
     L = max(seq, 0);
-  } else if constexpr (F == kWindow) {  // columns [lo, hi) of the row, clamped to it
+  } else if constexpr (form_of(F) == kWindow) {  // columns [lo, hi) of the row, clamped to it
     const int64_t hi = min(static_cast<int64_t>(max(seq, 0)), p.row_stride);
     const int64_t lo = min(static_cast<int64_t>(max(start, 0)), hi);
     m.rstart = static_cast<int32_t>(lo);
@@ -1262,14 +1305,21 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     rowp = p.scores + static_cast<int64_t>(row) * p.row_stride;
     L = static_cast<int32_t>(min(static_cast<int64_t>(max(seq, 0)), p.row_stride));
   }
-  if constexpr (F == kPaged) m.pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+  if constexpr (form_of(F) == kPaged) m.pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
   const int32_t k = p.k;
   int32_t* out = p.out + static_cast<int64_t>(row) * k;
 
   if (L <= k) {  // every position is selected; the rest of the row is -1
     const int32_t s0 = static_cast<int32_t>(static_cast<int64_t>(k) * rank / G);
     const int32_t s1 = static_cast<int32_t>(static_cast<int64_t>(k) * (rank + 1) / G);
-    for (int32_t i = s0 + tid; i < s1; i += kThreads) out[i] = i < L ? map_pos<F>(m, i) : -1;
+    const bool keys = opts_of(F) && (m.values != nullptr || m.staged != nullptr);
+    for (int32_t i = s0 + tid; i < s1; i += kThreads) {
+      if (i < L)
+        emit<F>(out, k, static_cast<uint32_t>(i), m, i,
+                keys ? order_key(__float_as_uint(rowp[i])) : 0u);
+      else
+        emit_pad<F>(out, static_cast<uint32_t>(i), m);
+    }
     return;
   }
 
@@ -1280,7 +1330,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // to shared memory asynchronously (waited for after the sample); the other CTAs
   // of a cluster, and rows of more than kPtCap pages, read it from global memory
   int32_t pages = 0;
-  if constexpr (F == kPaged) {
+  if constexpr (form_of(F) == kPaged) {
     const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
     const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
     if (rank == 0 && np <= kPtCap) {
@@ -1303,7 +1353,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     const uint32_t lambda =
         sampled ? sample_lambda(sm, s, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl, &shift2)
                 : 0u;
-    if constexpr (F == kPaged) {
+    if constexpr (form_of(F) == kPaged) {
       if (pages > 0) {
         cp_async_wait_all();
         m.pt_smem = pt_smem;  // visible to all threads after the next barrier
@@ -1354,7 +1404,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   }
 
   // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
-  if constexpr (F == kPaged) {
+  if constexpr (form_of(F) == kPaged) {
     if (pages > 0 && m.pt_smem == nullptr) {  // the fast tier did not run
       cp_async_wait_all();
       __syncthreads();
@@ -1459,6 +1509,71 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   row_body<F>(prob, item - gp.row_begin[i], G, static_cast<int>(cluster_ctarank()), dyn, ctl);
 }
 
+// The sort pass of the sorted output (one CTA per row, after the selection kernel):
+// the row's k staged (key, position) pairs are ordered by the composite (key,
+// ~position), largest first, so equal keys come by smaller position first and the
+// padding pairs (composite 0) last, with a bitonic network in shared memory; then
+// out (mapped) and values are written in that order.
+constexpr int kSortMax = 2048;  // the largest k
+template <int F>
+__global__ void __launch_bounds__(kThreads) topk_sort_kernel(const Params p) {
+  __shared__ uint64_t v[kSortMax];
+  const int row = static_cast<int>(blockIdx.x);
+  const int tid = threadIdx.x;
+  const int k = p.k;
+  int n = 1;
+  while (n < k) n <<= 1;
+  const uint2* st = p.staged + static_cast<int64_t>(row) * k;
+  for (int i = tid; i < n; i += kThreads) {
+    uint64_t c = 0;
+    if (i < k) {
+      const uint2 e = st[i];
+      c = (static_cast<uint64_t>(e.x) << 32) | static_cast<uint64_t>(~e.y);
+    }
+    v[i] = c;
+  }
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = tid; i < n; i += kThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const uint64_t a = v[i], b = v[j];
+          const bool desc = (i & size) == 0;  // this run is ordered largest first
+          if (desc ? a < b : a > b) {
+            v[i] = b;
+            v[j] = a;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  OutMap m;
+  m.pt_row = form_of(F) == kPaged ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
+  m.pt_smem = nullptr;
+  m.ps = p.page_size;
+  m.ps_shift = p.page_shift;
+  m.rstart = 0;
+  m.values = p.values != nullptr ? p.values + static_cast<int64_t>(row) * k : nullptr;
+  m.staged = nullptr;
+  if constexpr (form_of(F) == kRagged) {
+    m.rstart = p.row_starts[row];
+  } else if constexpr (form_of(F) == kWindow) {  // the window's first column, as the selection took it
+    const int64_t hi = min(static_cast<int64_t>(max(p.seq_lens[row], 0)), p.row_stride);
+    m.rstart = static_cast<int32_t>(min(static_cast<int64_t>(max(p.row_starts[row], 0)), hi));
+  }
+  int32_t* out = p.out + static_cast<int64_t>(row) * k;
+  for (int i = tid; i < k; i += kThreads) {
+    const uint64_t c = v[i];
+    if (c == 0)
+      emit_pad<F>(out, static_cast<uint32_t>(i), m);
+    else
+      emit<F>(out, k, static_cast<uint32_t>(i), m, static_cast<int32_t>(~static_cast<uint32_t>(c)),
+              static_cast<uint32_t>(c >> 32));
+  }
+}
+
 template <class Kernel, class Arg>
 cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, int tie_cap,
                             cudaStream_t stream) {
@@ -1498,8 +1613,9 @@ cudaError_t prepare_kernel(Kernel kernel) {
 
 template <int F>
 cudaError_t prepare_form() {
-  const cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
-  return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F>) : e;
+  cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
+  if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F>);
+  return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F | kOpts>) : e;
 }
 
 }  // namespace
@@ -1527,7 +1643,36 @@ cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream) {
+template <int F>
+cudaError_t sort_form(const Params& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, topk_sort_kernel<F>, p);
+}
+
+cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {
+  switch (form) {
+    case kRaw: return sort_form<kRaw | kOpts>(p, stream);
+    case kPaged: return sort_form<kPaged | kOpts>(p, stream);
+    case kRagged: return sort_form<kRagged | kOpts>(p, stream);
+    case kWindow: return sort_form<kWindow | kOpts>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,
+                         cudaStream_t stream) {
+  if (opts) {
+    switch (form) {
+      case kRaw: return launch_group_form<kRaw | kOpts>(gp, g, stream);
+      case kPaged: return launch_group_form<kPaged | kOpts>(gp, g, stream);
+      case kRagged: return launch_group_form<kRagged | kOpts>(gp, g, stream);
+      case kWindow: return launch_group_form<kWindow | kOpts>(gp, g, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (form) {
     case kRaw: return launch_group_form<kRaw>(gp, g, stream);
     case kPaged: return launch_group_form<kPaged>(gp, g, stream);

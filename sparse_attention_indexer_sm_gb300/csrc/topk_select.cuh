@@ -24,6 +24,9 @@ struct Params {
   int32_t page_size;
   int32_t page_shift;          // log2(page_size) when it is a power of two, else -1
   int32_t* out;                // [batch, k]
+  float* values;               // [batch, k] or null: each slot's score, -inf in padding slots
+  uint2* staged;               // [batch, k] or null: (key, position) per slot instead of out
+                               // and values, for the sort pass (sort_rows) to order and write
   int32_t k;
   int32_t tie_cap;             // <= kTieCapMax
   int32_t batch;
@@ -53,8 +56,13 @@ constexpr int kTieCap256 = 3072;
   /* Enqueue the kernel: grid = batch * g CTAs in clusters of g along x. */             \
   cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);           \
   /* Enqueue one launch over every row of the group's problems (all of `form`, with */  \
-  /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. */               \
-  cudaError_t launch_group(Form form, const GroupParams& gp, int g, cudaStream_t stream);
+  /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. opts: some */    \
+  /* problem has the values output or the sorted option (staged). */                    \
+  cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,          \
+                           cudaStream_t stream);                                        \
+  /* The sort pass of the sorted output: p.staged (filled by a launch with p) is */     \
+  /* ordered per row and written to p.out and p.values; one CTA per row. */             \
+  cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);
 
 namespace cta512 {
 TOPK_CTA_INTERFACE

@@ -97,6 +97,19 @@ def test_grouped_layout_and_host_checks(lib):
                            out=one)) == 1                                 # window without starts
     assert group(P(form=0, batch=1, k=4, row_stride=8, scores=18, seq_lens=one,
                    out=one)) == 1                                         # misaligned scores
+    assert group(P(form=0, batch=1, k=4, row_stride=8, scores=one, seq_lens=one, out=one,
+                   flags=2)) == 1                                         # unknown flag
+    sorted_raw = P(form=0, batch=3, k=100, row_stride=8, scores=one, seq_lens=one, out=one,
+                   flags=pkg.TOPK_FLAG_SORTED)
+    arr = (P * 2)(ok_raw, sorted_raw)
+    need = lib.topk_problem_workspace_bytes(ctypes.addressof(arr), 2)
+    assert need == 2560  # 3 * 100 pairs of 8 bytes, rounded up to 256
+    assert lib.topk_problem_workspace_bytes(ctypes.addressof(arr), 1) == 0
+    assert lib.topk_transform_grouped(ctypes.addressof(arr), 2, None, 0, None) == 3
+    assert lib.topk_transform_grouped(ctypes.addressof(arr), 2, ctypes.c_void_p(256), need - 1,
+                                      None) == 3
+    assert lib.topk_transform_grouped(ctypes.addressof(arr), 2, ctypes.c_void_p(260), need,
+                                      None) == 1                         # misaligned workspace
 
 
 def test_cta_threads_control_round_trip(lib):

@@ -576,3 +576,69 @@ def test_all_equal_rows_cta256(pkg, split):
     with settings(pkg, split=split, cta=256):
         got = run_gpu(pkg, w)
     assert_parity(w, got)
+
+
+# ------------------------------------------------------------ values and sorted output
+
+def run_options(pkg, ws, sorted_=False):
+    """Grouped call with the values output (and the sorted option) on every problem."""
+    dev = torch.device("cuda:0")
+    probs = []
+    for w in ws:
+        q = problem_of(w, dev)
+        q["values"] = torch.full((w.batch, w.k), 7.0, dtype=torch.float32, device=dev)  # poison
+        q["sorted"] = sorted_
+        probs.append(q)
+    outs = pkg.topk_transform_grouped(probs)
+    torch.cuda.synchronize()
+    return [(o.cpu().numpy(), q["values"].cpu().numpy()) for o, q in zip(outs, probs)]
+
+
+def assert_options(w, got, vals, sorted_):
+    exp, exp_vals = oracle.run_values(w)
+    if sorted_:  # rank order and values, slot by slot
+        bad = np.flatnonzero(~(got == exp).all(axis=1))
+        assert bad.size == 0, f"{w.name}: row {bad[0]} order {got[bad[0]][:8]} vs {exp[bad[0]][:8]}"
+        assert (vals.view(np.uint32) == exp_vals.view(np.uint32)).all(), f"{w.name}: values differ"
+    else:  # the set, and each slot's value belongs to its position
+        assert_parity(w, got)
+        order_got, order_exp = np.argsort(got, axis=1), np.argsort(exp, axis=1)
+        v_got = np.take_along_axis(vals, order_got, 1).view(np.uint32)
+        v_exp = np.take_along_axis(exp_vals, order_exp, 1).view(np.uint32)
+        assert (v_got == v_exp).all(), f"{w.name}: values do not follow their positions"
+
+
+def option_workloads():
+    g = np.random.Generator(np.random.PCG64(71))
+    ties = workloads.Workload("opt_ties", "raw", 300, np.round(
+        workloads.random_rows(g, 5, 3000, "normal"), 1).astype(np.float32),
+        np.array([3000, 2999, 200, 0, 2500], np.int32))
+    return [workloads.config1(), workloads.config2(8192, batch=12), workloads.config3(8, "raw"),
+            workloads.config4("narrow", batch=3), workloads.prefill_windows(64, 4096, window=1500),
+            ties, workloads.config5(1)]
+
+
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_values_and_sorted_output(pkg, sorted_):
+    ws = option_workloads()
+    for w, (got, vals) in zip(ws, run_options(pkg, ws, sorted_)):
+        assert_options(w, got, vals, sorted_)
+
+
+@pytest.mark.parametrize("cta", [256, 512])
+@pytest.mark.parametrize("fast", [1, 0])
+@pytest.mark.parametrize("split", [1, 4])
+def test_sorted_output_every_path(pkg, cta, fast, split):
+    ws = [_mixed(300 + split, "banded", batch=4), _mixed(301, "narrow", batch=3, k=2048),
+          many_rows("paged", 40, 5000, 1000, 73)]
+    with settings(pkg, cta=cta, fast=fast, split=split):
+        outs = run_options(pkg, ws, True)
+    for w, (got, vals) in zip(ws, outs):
+        assert_options(w, got, vals, True)
+
+
+@pytest.mark.parametrize("k", [1, 2, 1023, 2048])
+def test_sorted_any_k(pkg, k):
+    w = many_rows("raw", 6, 9000, k, 80 + k, "heavy_tail")
+    ((got, vals),) = run_options(pkg, [w], True)
+    assert_options(w, got, vals, True)
