@@ -196,6 +196,17 @@ size_t topk_problem_workspace_bytes(const topk_problem_t* problems, int32_t n_pr
 int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* As topk_transform_grouped, with no workspace argument: sorted problems stage
+ * their (key, position) pairs in a scratch array the library keeps in device
+ * memory (a static __device__ array of TOPK_STATIC_WORKSPACE_BYTES per device, part
+ * of the loaded module), so the call allocates nothing. Returns
+ * TOPK_ERR_WORKSPACE_TOO_SMALL, before any launch, when the problems need more
+ * than that (topk_problem_workspace_bytes). Calls that use the array must not
+ * overlap on a device: issue them on one stream, or order their streams. */
+#define TOPK_STATIC_WORKSPACE_BYTES (16u << 20)
+int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_problems,
+                                  cudaStream_t stream);
+
 /* A static English description of a status code. */
 const char* topk_status_string(int status);
 

@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_transform_grouped.argtypes = [vp, i32, vp, sz, vp]
             lib.topk_problem_bytes.restype = sz
             lib.topk_problem_bytes.argtypes = []
+            lib.topk_transform_grouped_static.restype = ctypes.c_int
+            lib.topk_transform_grouped_static.argtypes = [vp, i32, vp]
             lib.topk_problem_workspace_bytes.restype = sz
             lib.topk_problem_workspace_bytes.argtypes = [vp, i32]
             if lib.topk_problem_bytes() != ctypes.sizeof(TopkProblem):
@@ -250,7 +252,8 @@ class TopkProblem(ctypes.Structure):
 TOPK_FLAG_SORTED = 1
 
 
-def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tensor]:
+def topk_transform_grouped(problems: list[dict], stream=None,
+                           static_workspace: bool = False) -> list[torch.Tensor]:
     """Several independent transforms in one call (one launch per form present).
 
     Each problem is a dict with "form" ("raw", "paged", "ragged" or "window"), "k",
@@ -260,7 +263,9 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
     [batch, k] fp32 device tensor that receives each slot's score (-inf in the
     padding slots), and "sorted": True for the slots in rank order (largest score
     first, equal scores by smaller position first). Sorted problems use a device
-    workspace this function allocates. Returns the output tensors, in order."""
+    workspace this function allocates, or, with static_workspace=True, the
+    library's own scratch array (no allocation; such calls must not overlap on a
+    device). Returns the output tensors, in order."""
     lib = load_library()
     if len(problems) > TOPK_MAX_GROUP:
         raise ValueError(f"at most {TOPK_MAX_GROUP} problems per grouped call")
@@ -317,6 +322,12 @@ def topk_transform_grouped(problems: list[dict], stream=None) -> list[torch.Tens
         arr[i].scores, arr[i].seq_lens, arr[i].out = scores.data_ptr(), q["seq_lens"].data_ptr(), out.data_ptr()
         outs.append(out)
     if not problems:
+        return outs
+    if static_workspace:
+        with torch.cuda.device(dev):
+            st = lib.topk_transform_grouped_static(ctypes.addressof(arr), len(problems),
+                                                   _stream(stream, dev))
+        _check(st, "topk_transform_grouped_static")
         return outs
     ws_bytes = int(lib.topk_problem_workspace_bytes(ctypes.addressof(arr), len(problems)))
     with torch.cuda.device(dev):

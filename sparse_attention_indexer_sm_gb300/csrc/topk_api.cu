@@ -23,6 +23,9 @@ std::atomic<int> g_row_split{kRowSplitUnset};
 std::atomic<int> g_tie_cap{topk_gb300::kTieCapMax};
 std::atomic<int> g_fast_tier{1};
 std::atomic<int> g_cta_threads{0};  // 0: automatic; 512 or 256: that build
+
+// The scratch of topk_transform_grouped_static: part of the module, one per device.
+static __device__ __align__(256) unsigned char g_static_stage[TOPK_STATIC_WORKSPACE_BYTES];
 thread_local int t_last_cuda_error = 0;
 
 struct DeviceState {
@@ -341,6 +344,23 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return TOPK_OK;
+}
+
+int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_problems,
+                                  cudaStream_t stream) {
+  if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
+  if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  const size_t need = staging_bytes(problems, n_problems, nullptr);
+  if (need > TOPK_STATIC_WORKSPACE_BYTES) return TOPK_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  if (need > 0) {
+    DeviceState* ds = nullptr;  // loads the module on this device first
+    const int st = device_state(&ds);
+    if (st != TOPK_OK) return st;
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_static_stage);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return topk_transform_grouped(problems, n_problems, scratch, need > 0 ? need : 0, stream);
 }
 
 const char* topk_status_string(int status) {

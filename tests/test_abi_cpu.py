@@ -110,6 +110,13 @@ def test_grouped_layout_and_host_checks(lib):
                                       None) == 3
     assert lib.topk_transform_grouped(ctypes.addressof(arr), 2, ctypes.c_void_p(260), need,
                                       None) == 1                         # misaligned workspace
+    # the static-scratch call: more staging than the library's array holds
+    big = P(form=0, batch=(16 << 20) // (8 * 2048) + 1, k=2048, row_stride=8, scores=one,
+            seq_lens=one, out=one, flags=pkg.TOPK_FLAG_SORTED)
+    arr1 = (P * 1)(big)
+    assert lib.topk_transform_grouped_static(ctypes.addressof(arr1), 1, None) == 3
+    assert lib.topk_transform_grouped_static(None, 1, None) == 1
+    assert lib.topk_transform_grouped_static(None, 0, None) == 0
 
 
 def test_cta_threads_control_round_trip(lib):

@@ -580,7 +580,7 @@ def test_all_equal_rows_cta256(pkg, split):
 
 # ------------------------------------------------------------ values and sorted output
 
-def run_options(pkg, ws, sorted_=False):
+def run_options(pkg, ws, sorted_=False, static_workspace=False):
     """Grouped call with the values output (and the sorted option) on every problem."""
     dev = torch.device("cuda:0")
     probs = []
@@ -589,7 +589,7 @@ def run_options(pkg, ws, sorted_=False):
         q["values"] = torch.full((w.batch, w.k), 7.0, dtype=torch.float32, device=dev)  # poison
         q["sorted"] = sorted_
         probs.append(q)
-    outs = pkg.topk_transform_grouped(probs)
+    outs = pkg.topk_transform_grouped(probs, static_workspace=static_workspace)
     torch.cuda.synchronize()
     return [(o.cpu().numpy(), q["values"].cpu().numpy()) for o, q in zip(outs, probs)]
 
@@ -642,3 +642,23 @@ def test_sorted_any_k(pkg, k):
     w = many_rows("raw", 6, 9000, k, 80 + k, "heavy_tail")
     ((got, vals),) = run_options(pkg, [w], True)
     assert_options(w, got, vals, True)
+
+
+def test_sorted_output_static_workspace(pkg):
+    """The call that stages in the library's own scratch array: same results; twice
+    in a row on one stream (the array is reused)."""
+    ws = option_workloads()
+    for _ in range(2):
+        for w, (got, vals) in zip(ws, run_options(pkg, ws, True, static_workspace=True)):
+            assert_options(w, got, vals, True)
+
+
+def test_static_workspace_too_small(pkg):
+    dev = torch.device("cuda:0")
+    B, k = (16 << 20) // (8 * 2048) + 1, 2048
+    w = workloads.Workload("too_big", "raw", k, np.zeros((B, 8), np.float32),
+                           np.full(B, 8, np.int32))
+    q = problem_of(w, dev)
+    q["sorted"] = True
+    with pytest.raises(pkg.TopkError):
+        pkg.topk_transform_grouped([q], static_workspace=True)
