@@ -40,6 +40,14 @@
  * the -1 padding, so it need not be pre-filled. The first call on a device sets
  * kernel attributes on that device; make it before capturing a CUDA graph.
  *
+ * Stream order: every launch allows programmatic dependent launch, so it may be
+ * scheduled while the previous kernel of the stream is still running, and it lets
+ * the next kernel of the stream do the same. Before it reads or writes any buffer
+ * it waits until the previous kernel has completed and its memory is visible
+ * (griddepcontrol.wait), so the usual stream ordering of data holds. A kernel
+ * that follows in the stream and was itself launched with programmatic
+ * serialization must wait the same way before it reads `out`.
+ *
  * Layouts (all row-major, int32 unless stated):
  *   scores      fp32, 4-byte aligned. raw/paged: row b starts at
  *               scores + b * row_stride (elements); ragged: row b starts at

@@ -165,6 +165,18 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return r;
 }
 
+// Programmatic dependent launch: every launch lets the next kernel of the stream be
+// scheduled before it ends. allow_next_grid signals that (early, from every
+// thread); wait_prior_grids returns once the previous kernel of the stream has
+// completed and its memory is visible. Each kernel calls it before it reads or
+// writes any buffer, so only shared-memory set-up overlaps the previous kernel.
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Full cluster barrier; release/acquire orders shared-memory traffic across CTAs.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(
@@ -1245,6 +1257,25 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
       reinterpret_cast<uint2*>(dyn + (G > 1 ? 2 : 1) * kHistWords + kListWords + kPtCap);
   const uint32_t cap = static_cast<uint32_t>(p.tie_cap);
 
+  allow_next_grid();
+  // independent of the row: clear the histograms and counters (overlapping the
+  // previous kernel's tail), then wait for it before touching any buffer
+  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (G > 1 && rank == 0)
+    for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
+  if (tid == 0) {
+    ctl.win_cnt = 0;
+    ctl.tie_cnt = 0;
+    ctl.out_cnt = 0;
+    ctl.cand_cnt = 0;
+    ctl.ns = 0;
+    ctl.cls_cnt = 0;
+    ctl.lambda = 0;
+    ctl.lambda_shift = 0;
+  }
+
+  wait_prior_grids();
+
   // the row's length (and start) first: everything waits for them
   const int32_t seq = p.seq_lens[row];
   int32_t start = 0;  // ragged: row offset; window: window start
@@ -1261,22 +1292,6 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
                   sm);
       sample_loaded = true;
     }
-  }
-
-  // independent of the row: clear the histograms and counters while those loads
-  // are in flight
-  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
-  if (G > 1 && rank == 0)
-    for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
-  if (tid == 0) {
-    ctl.win_cnt = 0;
-    ctl.tie_cnt = 0;
-    ctl.out_cnt = 0;
-    ctl.cand_cnt = 0;
-    ctl.ns = 0;
-    ctl.cls_cnt = 0;
-    ctl.lambda = 0;
-    ctl.lambda_shift = 0;
   }
 
   OutMap m;
@@ -1521,6 +1536,8 @@ __global__ void __launch_bounds__(kThreads) topk_sort_kernel(const Params p) {
   const int row = static_cast<int>(blockIdx.x);
   const int tid = threadIdx.x;
   const int k = p.k;
+  allow_next_grid();
+  wait_prior_grids();  // the staged pairs come from the selection kernel
   int n = 1;
   while (n < k) n <<= 1;
   const uint2* st = p.staged + static_cast<int64_t>(row) * k;
@@ -1582,13 +1599,15 @@ cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(g, tie_cap);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(g);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, arg);
 }
 
@@ -1649,6 +1668,11 @@ cudaError_t sort_form(const Params& p, cudaStream_t stream) {
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, topk_sort_kernel<F>, p);
 }
 
