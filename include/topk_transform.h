@@ -221,6 +221,15 @@ const char* topk_status_string(int status);
 /* The cudaError_t of the last TOPK_ERR_CUDA returned on this host thread. */
 int topk_last_cuda_error(void);
 
+/* Diagnostics. Every write the kernels make into a row's output, the tie list or
+ * the tie buffer is guarded by a check that consistent inputs never fail (it can
+ * fail only if inputs change while a kernel runs, or through a bug); a failed check
+ * skips the write and is counted on the device instead of trapping.
+ * topk_guard_hits(&n) reads the count on the current device (synchronously: it
+ * waits for the device's pending work); topk_reset_guard_hits() sets it to 0. */
+int topk_guard_hits(uint64_t* hits);
+int topk_reset_guard_hits(void);
+
 /* Tuning and test controls (process-wide; each returns the previous value).
  *
  * topk_set_row_split(g): number of CTAs (a thread-block cluster) that share one

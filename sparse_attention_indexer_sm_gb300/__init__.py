@@ -27,7 +27,7 @@ __all__ = [
     "TopkError", "TOPK_MAX_K", "TOPK_TIE_CAPACITY_MAX", "library_path", "load_library",
     "topk_transform_raw", "topk_transform_paged", "topk_transform_ragged", "topk_transform_window",
     "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "TOPK_FLAG_SORTED",
-    "topk_set_cta_threads",
+    "topk_set_cta_threads", "topk_guard_hits", "topk_reset_guard_hits",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
 ]
 
@@ -90,6 +90,10 @@ def load_library() -> ctypes.CDLL:
             lib.topk_set_row_split.argtypes = [ctypes.c_int]
             lib.topk_set_tie_capacity.restype = ctypes.c_int
             lib.topk_set_tie_capacity.argtypes = [ctypes.c_int]
+            lib.topk_guard_hits.restype = ctypes.c_int
+            lib.topk_guard_hits.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+            lib.topk_reset_guard_hits.restype = ctypes.c_int
+            lib.topk_reset_guard_hits.argtypes = []
             lib.topk_set_cta_threads.restype = ctypes.c_int
             lib.topk_set_cta_threads.argtypes = [ctypes.c_int]
             lib.topk_set_fast_tier.restype = ctypes.c_int
@@ -349,6 +353,18 @@ def topk_set_row_split(g: int) -> int:
 def topk_set_tie_capacity(cap: int) -> int:
     """Entries of the shared tie buffer (0 .. TOPK_TIE_CAPACITY_MAX); for tests."""
     return int(load_library().topk_set_tie_capacity(int(cap)))
+
+
+def topk_guard_hits() -> int:
+    """Failed internal consistency checks on the current device (0 unless inputs
+    changed while a kernel ran, or a bug); waits for the device's pending work."""
+    n = ctypes.c_uint64(0)
+    _check(load_library().topk_guard_hits(ctypes.byref(n)), "topk_guard_hits")
+    return int(n.value)
+
+
+def topk_reset_guard_hits() -> None:
+    _check(load_library().topk_reset_guard_hits(), "topk_reset_guard_hits")
 
 
 def topk_set_cta_threads(threads: int) -> int:

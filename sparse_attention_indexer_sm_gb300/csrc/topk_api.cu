@@ -376,6 +376,28 @@ const char* topk_status_string(int status) {
 
 int topk_last_cuda_error(void) { return t_last_cuda_error; }
 
+int topk_guard_hits(uint64_t* hits) {
+  if (hits == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != TOPK_OK) return st;
+  unsigned int a = 0, b = 0;
+  cudaError_t e = topk_gb300::cta512::guard_hits(&a);
+  if (e == cudaSuccess) e = topk_gb300::cta256::guard_hits(&b);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *hits = static_cast<uint64_t>(a) + b;
+  return TOPK_OK;
+}
+
+int topk_reset_guard_hits(void) {
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != TOPK_OK) return st;
+  cudaError_t e = topk_gb300::cta512::reset_guard_hits();
+  if (e == cudaSuccess) e = topk_gb300::cta256::reset_guard_hits();
+  return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
+}
+
 int topk_set_row_split(int g) {
   const int prev = row_split_setting();
   g_row_split.store(g < 1 ? 0 : g, std::memory_order_relaxed);

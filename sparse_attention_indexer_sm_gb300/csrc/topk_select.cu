@@ -165,6 +165,13 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return r;
 }
 
+// Internal consistency checks that consistent inputs never fail (a failure means
+// the scores changed while a kernel ran, or a bug) skip the access they guard and
+// are counted here, instead of trapping, so that the host can read the count
+// (guard_hits) and the context stays usable.
+__device__ unsigned int g_guard_hits;
+__device__ __forceinline__ void guard_hit() { atomicAdd(&g_guard_hits, 1u); }
+
 // Programmatic dependent launch: every launch lets the next kernel of the stream be
 // scheduled before it ends. allow_next_grid signals that (early, from every
 // thread); wait_prior_grids returns once the previous kernel of the stream has
@@ -599,7 +606,7 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
 template <int F>
 __device__ __forceinline__ void emit(int32_t* out, int32_t k, uint32_t slot, const OutMap& m,
                                      int32_t j, uint32_t key) {
-  if (slot >= static_cast<uint32_t>(k)) return;
+  if (slot >= static_cast<uint32_t>(k)) return;  // the callers' checks count misses
   if constexpr (opts_of(F)) {
     if (m.staged != nullptr) {
       m.staged[slot] = make_uint2(key, static_cast<uint32_t>(j));
@@ -1023,7 +1030,10 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
       // Composites are unique (positions are), so the loop ends with the threshold
       // bin holding exactly what is still needed, at the latest when p reaches 0;
       // the test below only bounds the loop should that ever not hold.
-      if (p <= 0) break;
+      if (p <= 0) {
+        if (tid == 0) guard_hit();
+        break;
+      }
       const int lo = p > 32 ? 32 : 0;
       const int w = min(kBufRoundBits, p - lo);
       const int np = p - w;
@@ -1054,7 +1064,12 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
       sel = hi_bits(compose(e), p) >= P;
     }
     const uint32_t slot = warp_reserve_bit(&ctl.out_cnt, sel);
-    if (sel && slot < want) emit<F>(out, k, k_above + slot, m, static_cast<int32_t>(e.y), e.x);
+    if (sel) {
+      if (slot < want)
+        emit<F>(out, k, k_above + slot, m, static_cast<int32_t>(e.y), e.x);
+      else
+        guard_hit();
+    }
   }
 }
 
@@ -1106,10 +1121,15 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
       if (ws < above) {
         const uint2 e = buf[i];
         emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y), e.x);
+      } else {
+        guard_hit();
       }
       ++ws;
     } else if (c == 2u) {
-      if (ts < ct) list[ts] = buf[i];
+      if (ts < ct)
+        list[ts] = buf[i];
+      else
+        guard_hit();
       ++ts;
     }
   }
@@ -1145,7 +1165,10 @@ __device__ __forceinline__ void scatter_pass(const Slice& s, uint32_t prefix, in
                                              uint32_t cap, const OutMap& m, Ctl& ctl) {
   const int tid = threadIdx.x;
   auto put_tie = [&](uint32_t slot, uint32_t key, int32_t j) {
-    if (slot >= cap) return;
+    if (slot >= cap) {
+      guard_hit();
+      return;
+    }
     if (remote)
       dsmem_st2(ties_remote + 8u * slot, key, static_cast<uint32_t>(j));
     else
@@ -1674,6 +1697,15 @@ cudaError_t sort_form(const Params& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, topk_sort_kernel<F>, p);
+}
+
+cudaError_t guard_hits(unsigned int* hits) {
+  return cudaMemcpyFromSymbol(hits, g_guard_hits, sizeof(unsigned int));
+}
+
+cudaError_t reset_guard_hits() {
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_guard_hits, &zero, sizeof(unsigned int));
 }
 
 cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {

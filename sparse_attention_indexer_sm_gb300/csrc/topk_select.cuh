@@ -62,7 +62,11 @@ constexpr int kTieCap256 = 3072;
                            cudaStream_t stream);                                        \
   /* The sort pass of the sorted output: p.staged (filled by a launch with p) is */     \
   /* ordered per row and written to p.out and p.values; one CTA per row. */             \
-  cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);
+  cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);                \
+  /* The count of failed internal consistency checks on the current device (a */       \
+  /* synchronous read), and its reset. */                                               \
+  cudaError_t guard_hits(unsigned int* hits);                                           \
+  cudaError_t reset_guard_hits();
 
 namespace cta512 {
 TOPK_CTA_INTERFACE

@@ -30,6 +30,14 @@ def pkg():
     return p
 
 
+@pytest.fixture(autouse=True)
+def no_guard_hits(pkg):
+    """No internal consistency check of the kernels fails in any test."""
+    pkg.topk_reset_guard_hits()
+    yield
+    assert pkg.topk_guard_hits() == 0, "a kernel's internal consistency check failed"
+
+
 @contextlib.contextmanager
 def settings(pkg, split=None, tie_cap=None, fast=None, cta=None):
     prev_split = pkg.topk_set_row_split(split) if split is not None else None
