@@ -85,7 +85,7 @@ constexpr int kCtasPerSm = 1024 / kThreads;  // at 64 registers per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;            // 128-bit loads in flight per thread per step (exact tier)
 constexpr int kFilterUnroll = 8;      // 128-bit loads in flight per thread in the filter
-constexpr int kMaskIters = 4;         // filter iterations whose masks are decoded together
+constexpr int kMaskIters = 2;         // filter iterations whose masks are decoded together
 constexpr int kRowRoundBits = 12;     // histogram width of the rounds over the row
 constexpr int kBufRoundBits = 12;     // histogram width of the rounds over a buffer
 constexpr int kSampleQuads = 512 / kThreads;  // sampled 16-byte quads per thread (2048 keys per CTA)
