@@ -570,6 +570,8 @@ struct OutMap {
 // The kernels' template argument F is a Form, plus kOpts when the launch has the
 // values output or the sorted option (so that launches without them carry neither).
 constexpr int kOpts = 4;
+// ... and kSingle for launches of one CTA per row (no cluster code at all)
+constexpr int kSingle = 8;
 __host__ __device__ constexpr int form_of(int F) { return F & 3; }
 __host__ __device__ constexpr bool opts_of(int F) { return (F & kOpts) != 0; }
 
@@ -1519,14 +1521,18 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   }
 }
 
-// One cluster of G CTAs per row.
+// One cluster of G CTAs per row (with kSingle: one CTA, G = 1 at compile time).
 template <int F>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_rows_kernel(const Params p) {
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Ctl ctl;
-  const int G = static_cast<int>(cluster_nctarank());
-  row_body<F>(p, static_cast<int>(blockIdx.x) / G, G, static_cast<int>(cluster_ctarank()), dyn,
-              ctl);
+  if constexpr ((F & kSingle) != 0) {
+    row_body<F>(p, static_cast<int>(blockIdx.x), 1, 0, dyn, ctl);
+  } else {
+    const int G = static_cast<int>(cluster_nctarank());
+    row_body<F>(p, static_cast<int>(blockIdx.x) / G, G, static_cast<int>(cluster_ctarank()), dyn,
+                ctl);
+  }
 }
 
 // Several problems of one form in one launch: the clusters take the problems' rows
@@ -1636,6 +1642,7 @@ cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, 
 
 template <int F>
 cudaError_t launch_form(const Params& p, int g, cudaStream_t stream) {
+  if (g == 1) return launch_clusters(topk_rows_kernel<F | kSingle>, p, p.batch, 1, p.tie_cap, stream);
   return launch_clusters(topk_rows_kernel<F>, p, p.batch, g, p.tie_cap, stream);
 }
 
@@ -1656,6 +1663,7 @@ cudaError_t prepare_kernel(Kernel kernel) {
 template <int F>
 cudaError_t prepare_form() {
   cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
+  if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F>);
   return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F | kOpts>) : e;
 }
