@@ -76,15 +76,15 @@ int choose_split(int64_t batch, int64_t row_len, int sm_count) {
 
 // Launches of more rows than two 512-thread CTAs per SM hold take the 256-thread
 // build (four CTAs per SM, so each SM overlaps more rows) when one CTA owns a row,
-// the rows are at most 16384 elements (measured: faster at 8192, even at 16384,
-// slower at 32768, where half the threads per row lengthen each row's chain more
-// than the extra rows hide) and every problem's candidates fit that build's
-// smaller buffer (k <= 1024). row_len <= 0 means unknown.
+// the rows are at most 8192 elements (measured: faster at 8192, slower at 16384
+// and 32768, where half the threads per row lengthen each row's chain more than
+// the extra rows hide) and every problem's candidates fit that build's smaller
+// buffer (k <= 1024). row_len <= 0 means unknown.
 bool use_cta256(int64_t rows, int64_t row_len, int g, int32_t k_max, int sm_count) {
   const int forced = g_cta_threads.load(std::memory_order_relaxed);
   if (forced != 0) return forced == 256;
   return g == 1 && rows > 2 * static_cast<int64_t>(sm_count) && k_max <= 1024 &&
-         row_len > 0 && row_len <= 16384;
+         row_len > 0 && row_len <= 8192;
 }
 
 int fail_cuda(cudaError_t e) {
@@ -183,9 +183,12 @@ int run_one(const topk_problem_t& q, cudaStream_t stream) {
   cudaError_t e;
   if (use_cta256(p.batch, hint, g, p.k, ds->sm_count)) {
     p.tie_cap = std::min(p.tie_cap, topk_gb300::kTieCap256);
-    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, stream);
+    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, false, stream);
   } else {
-    e = topk_gb300::cta512::launch(static_cast<Form>(q.form), p, g, stream);
+    // more rows than SMs: SMs hold two CTAs and the candidates' L2 read-back
+    // contends, so the filter reads them back from L1 instead (measured)
+    e = topk_gb300::cta512::launch(static_cast<Form>(q.form), p, g, p.batch > ds->sm_count,
+                                   stream);
   }
   return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
 }

@@ -223,6 +223,16 @@ __device__ __forceinline__ void dsmem_st2(uint32_t addr, uint32_t a, uint32_t b)
 }
 
 // 128-bit read-only load that does not allocate in L1.
+// 128-bit read-only load that keeps its line in L1 (so that a candidate's value can
+// be read again from L1 right after).
+__device__ __forceinline__ uint4 ld_keep(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::evict_last.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -570,8 +580,11 @@ struct OutMap {
 // The kernels' template argument F is a Form, plus kOpts when the launch has the
 // values output or the sorted option (so that launches without them carry neither).
 constexpr int kOpts = 4;
-// ... and kSingle for launches of one CTA per row (no cluster code at all)
+// ... and kSingle for launches of one CTA per row (no cluster code at all), and
+// kKeysInFilter for single-CTA rows whose filter reads each candidate's value back
+// from L1 at once (instead of from L2 in a pass after the filter)
 constexpr int kSingle = 8;
+constexpr int kKeysInFilter = 16;
 __host__ __device__ constexpr int form_of(int F) { return F & 3; }
 __host__ __device__ constexpr bool opts_of(int F) { return (F & kOpts) != 0; }
 
@@ -821,22 +834,28 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
 }
 
 // F2, a row owned by one CTA: stream the row, keep per lane a 32-bit candidate
-// mask per iteration (8 quads), and every kMaskIters iterations turn the masks into
-// positions written compactly into the buffer (entry .y; .x is filled by
-// fill_candidates) at slots from one reservation per warp and group on the CTA's
-// counter (ctl.cand_cnt, zero on entry). Holding only masks lets the loads of a
-// whole group be in flight together. Slots at or beyond `cap` are counted but not
-// written.
-template <bool kPos>
-__device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint2* buf,
-                                                 uint32_t cap, Ctl& ctl) {
+// mask per iteration (8 quads), and every MI iterations turn the masks into
+// candidates written compactly into the buffer at slots from one reservation per
+// warp and group on the CTA's counter (ctl.cand_cnt, zero on entry). Holding only
+// masks lets the loads of a whole group be in flight together. Without kKeys only
+// positions are written (entry .y; fill_candidates reads the values back from L2
+// afterwards); with kKeys the loads keep their lines in L1, the masks are decoded
+// every iteration (MI = 1) and each candidate's value is read back from L1 at
+// once: the entry gets its key and the candidate histogram `chist` (bin =
+// min((key - lambda) >> shift, kFastBins - 1); zero on entry) its count. Slots at
+// or beyond `cap` are counted but not written.
+template <bool kPos, bool kKeys>
+__device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint32_t shift,
+                                                 uint2* buf, uint32_t cap, uint32_t* chist,
+                                                 Ctl& ctl) {
   const int tid = threadIdx.x;
   const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
   constexpr int U = kFilterUnroll;
-  constexpr int MI = kMaskIters;
+  constexpr int MI = kKeys ? 1 : kMaskIters;
   constexpr int32_t kStep = U * kThreads;
   int32_t ej;
   const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
+  uint32_t top = 0;  // kKeys: candidates in the last candidate-histogram bin
   bool first = true;
   for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
     uint32_t mk[MI];
@@ -849,7 +868,8 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int32_t q = base + u * kThreads + tid;
-          x[u] = q < s.nq ? ld_stream(s.vec + q) : make_uint4(0, 0, 0, 0);
+          x[u] = q < s.nq ? (kKeys ? ld_keep(s.vec + q) : ld_stream(s.vec + q))
+                          : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -869,7 +889,17 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
     uint32_t slot = warp_reserve(&ctl.cand_cnt, 0u, false, n);
     {
       auto put = [&](int32_t j) {
-        if (slot < cap) buf[slot].y = static_cast<uint32_t>(j);
+        if constexpr (kKeys) {
+          const uint32_t key = order_key(__float_as_uint(__ldg(s.row + j)));  // from L1
+          const uint32_t d = (key - lambda) >> shift;
+          if (d >= static_cast<uint32_t>(kFastBins - 1))
+            ++top;
+          else
+            atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+          if (slot < cap) buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
+        } else {
+          if (slot < cap) buf[slot].y = static_cast<uint32_t>(j);
+        }
         ++slot;
       };
       if (with_edge) put(ej);
@@ -885,6 +915,11 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
       }
     }
     first = false;
+  }
+  if constexpr (kKeys) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
+    if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kFastBins - 1)], top);
   }
 }
 
@@ -1402,13 +1437,14 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     uint32_t n_cand;
     uint32_t* chist = hist + kHC;
     if (G == 1) {
+      constexpr bool kKeys = (F & kKeysInFilter) != 0;
       if (lambda >= 0x80000000u)
-        filter_positions<true>(s, lambda, buf, cap, ctl);
+        filter_positions<true, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
       else
-        filter_positions<false>(s, lambda, buf, cap, ctl);
+        filter_positions<false, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
       __syncthreads();
       n_cand = ctl.cand_cnt;
-      if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
+      if (!kKeys && n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
         fill_candidates(rowp, buf, n_cand, lambda, shift2, chist, ctl);
     } else {
       const bool remote = rank != 0;
@@ -1641,7 +1677,10 @@ cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, 
 }
 
 template <int F>
-cudaError_t launch_form(const Params& p, int g, cudaStream_t stream) {
+cudaError_t launch_form(const Params& p, int g, bool keys_in_filter, cudaStream_t stream) {
+  if (g == 1 && keys_in_filter)
+    return launch_clusters(topk_rows_kernel<F | kSingle | kKeysInFilter>, p, p.batch, 1,
+                           p.tie_cap, stream);
   if (g == 1) return launch_clusters(topk_rows_kernel<F | kSingle>, p, p.batch, 1, p.tie_cap, stream);
   return launch_clusters(topk_rows_kernel<F>, p, p.batch, g, p.tie_cap, stream);
 }
@@ -1664,6 +1703,7 @@ template <int F>
 cudaError_t prepare_form() {
   cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
   if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle>);
+  if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F>);
   return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F | kOpts>) : e;
 }
@@ -1683,12 +1723,12 @@ cudaError_t prepare_device() {
   return e;
 }
 
-cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream) {
+cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter, cudaStream_t stream) {
   switch (form) {
-    case kRaw: return launch_form<kRaw>(p, g, stream);
-    case kPaged: return launch_form<kPaged>(p, g, stream);
-    case kRagged: return launch_form<kRagged>(p, g, stream);
-    case kWindow: return launch_form<kWindow>(p, g, stream);
+    case kRaw: return launch_form<kRaw>(p, g, keys_in_filter, stream);
+    case kPaged: return launch_form<kPaged>(p, g, keys_in_filter, stream);
+    case kRagged: return launch_form<kRagged>(p, g, keys_in_filter, stream);
+    case kWindow: return launch_form<kWindow>(p, g, keys_in_filter, stream);
   }
   return cudaErrorInvalidValue;
 }

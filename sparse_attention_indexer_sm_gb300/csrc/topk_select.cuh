@@ -53,8 +53,11 @@ constexpr int kTieCap256 = 3072;
   size_t smem_bytes(int g, int tie_cap);                                                \
   /* One-time per-device function attributes (max dynamic smem, cluster size 16). */    \
   cudaError_t prepare_device();                                                         \
-  /* Enqueue the kernel: grid = batch * g CTAs in clusters of g along x. */             \
-  cudaError_t launch(Form form, const Params& p, int g, cudaStream_t stream);           \
+  /* Enqueue the kernel: grid = batch * g CTAs in clusters of g along x. With g = 1, */  \
+  /* keys_in_filter picks the variant that reads candidates back from L1 in the */     \
+  /* filter (faster once SMs hold two CTAs each). */                                    \
+  cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter,            \
+                     cudaStream_t stream);                                              \
   /* Enqueue one launch over every row of the group's problems (all of `form`, with */  \
   /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. opts: some */    \
   /* problem has the values output or the sorted option (staged). */                    \
