@@ -333,9 +333,10 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     if (use_cta256(rows, hint, g, k_max, ds->sm_count)) {
       for (int i = 0; i < gp.n; ++i)
         gp.probs[i].tie_cap = std::min(gp.probs[i].tie_cap, topk_gb300::kTieCap256);
-      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts, stream);
+      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts, false, stream);
     } else {
-      e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, opts, stream);
+      e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, opts,
+                                           rows > ds->sm_count, stream);
     }
     if (e != cudaSuccess) return fail_cuda(e);
   }

@@ -1705,6 +1705,8 @@ cudaError_t prepare_form() {
   if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle>);
   if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F>);
+  if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kKeysInFilter>);
+  if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts | kKeysInFilter>);
   return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F | kOpts>) : e;
 }
 
@@ -1766,24 +1768,25 @@ cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,
-                         cudaStream_t stream) {
-  if (opts) {
-    switch (form) {
-      case kRaw: return launch_group_form<kRaw | kOpts>(gp, g, stream);
-      case kPaged: return launch_group_form<kPaged | kOpts>(gp, g, stream);
-      case kRagged: return launch_group_form<kRagged | kOpts>(gp, g, stream);
-      case kWindow: return launch_group_form<kWindow | kOpts>(gp, g, stream);
-    }
-    return cudaErrorInvalidValue;
-  }
+template <int Bits>
+cudaError_t launch_group_bits(Form form, const GroupParams& gp, int g, cudaStream_t stream) {
   switch (form) {
-    case kRaw: return launch_group_form<kRaw>(gp, g, stream);
-    case kPaged: return launch_group_form<kPaged>(gp, g, stream);
-    case kRagged: return launch_group_form<kRagged>(gp, g, stream);
-    case kWindow: return launch_group_form<kWindow>(gp, g, stream);
+    case kRaw: return launch_group_form<kRaw | Bits>(gp, g, stream);
+    case kPaged: return launch_group_form<kPaged | Bits>(gp, g, stream);
+    case kRagged: return launch_group_form<kRagged | Bits>(gp, g, stream);
+    case kWindow: return launch_group_form<kWindow | Bits>(gp, g, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,
+                         bool keys_in_filter, cudaStream_t stream) {
+  const bool keys = keys_in_filter && g == 1;
+  if (opts)
+    return keys ? launch_group_bits<kOpts | kKeysInFilter>(form, gp, g, stream)
+                : launch_group_bits<kOpts>(form, gp, g, stream);
+  return keys ? launch_group_bits<kKeysInFilter>(form, gp, g, stream)
+              : launch_group_bits<0>(form, gp, g, stream);
 }
 
 }  // namespace TOPK_CTA_NS

@@ -62,7 +62,7 @@ constexpr int kTieCap256 = 3072;
   /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. opts: some */    \
   /* problem has the values output or the sorted option (staged). */                    \
   cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,          \
-                           cudaStream_t stream);                                        \
+                           bool keys_in_filter, cudaStream_t stream);                   \
   /* The sort pass of the sorted output: p.staged (filled by a launch with p) is */     \
   /* ordered per row and written to p.out and p.values; one CTA per row. */             \
   cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);                \
