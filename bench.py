@@ -208,7 +208,7 @@ def device_sets(w, n_sets, dev, torch):
              "out": torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)}
         if w.form == "paged":
             d["pt"] = torch.from_numpy(w.page_table).to(dev)
-        if w.form == "window":
+        if w.form in ("window", "ragged"):
             d["starts"] = torch.from_numpy(w.row_starts).to(dev)
         sets.append(d)
     return sets
@@ -220,6 +220,9 @@ def call(pkg, w, d, stream):
                                  stream=stream)
     elif w.form == "window":
         pkg.topk_transform_window(d["scores"], d["starts"], d["seq"], w.k,
+                                  max_row_len_hint=w.max_row_len, out=d["out"], stream=stream)
+    elif w.form == "ragged":
+        pkg.topk_transform_ragged(d["scores"], d["starts"], d["seq"], w.k,
                                   max_row_len_hint=w.max_row_len, out=d["out"], stream=stream)
     else:
         pkg.topk_transform_raw(d["scores"], d["seq"], w.k, out=d["out"], stream=stream)
@@ -465,6 +468,20 @@ def run_ours(args):
             ab = algorithmic_bytes(b, C4_LEN, ws.k, form)
             sweep.append({"batch": b, "form": form, "us_per_call": pc * 1e6,
                           "rows_per_s": b / pc, "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
+                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+        # the other configurations of the workload table, each timed the same way
+        others = [("C1", workloads.config1()), ("C2 c4_len=8192", workloads.config2(8192)),
+                  ("C2 c4_len=32768", workloads.config2(32768))]
+        others += [(f"C4 {dist}", workloads.config4(dist)) for dist in ("banded", "narrow", "subnormal")]
+        others += [(f"C5 B={b}", workloads.config5(b)) for b in (1, 2, 4)]
+        for label, ws in others:
+            steps = 8192  # whole graph replays even for the smallest sets (4096 of them)
+            s, _, _, ns = time_steps(pkg, ws, steps, 5, dev, torch, l2)
+            pc = s / steps
+            ab = workload_bytes(ws)
+            sweep.append({"batch": ws.batch, "form": ws.form, "workload": f"{label}: {ws.name}",
+                          "us_per_call": pc * 1e6, "rows_per_s": ws.batch / pc,
+                          "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
                           "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
         # prefill-shaped window rows: 4096 queries over a 32768-key context, causal and
         # with a sliding window of 8192 keys
