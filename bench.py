@@ -419,7 +419,11 @@ def run_ours(args):
     traffic = profiled_traffic(w.batch, w.form)
 
     e2e_steps = max(20, min(args.steps, 400))
+    if dist is not None:
+        dist.barrier()
     e_secs, h2d, d2h = time_e2e(pkg, w, e2e_steps, dev, torch)
+    if dist is not None:  # the whole job's end-to-end rate: the slowest rank decides
+        e_secs = max_over_ranks(e_secs, dist, dev)
 
     result = {
         "metric": METRIC,
