@@ -670,3 +670,67 @@ def test_static_workspace_too_small(pkg):
     q["sorted"] = True
     with pytest.raises(pkg.TopkError):
         pkg.topk_transform_grouped([q], static_workspace=True)
+
+
+# ------------------------------------------------------------ graphs and streams
+
+def test_calls_captured_in_a_cuda_graph(pkg):
+    """Calls of every form captured in one CUDA graph (launches with programmatic
+    dependencies between them) and replayed give the oracle's results."""
+    dev = torch.device("cuda:0")
+    ws = [workloads.config3(64), workloads.config3(8, "raw"), workloads.config4("subnormal", batch=2),
+          workloads.prefill_windows(300, 6000, window=2500)]
+    probs = [problem_of(w, dev) for w in ws]
+    sorted_q = problem_of(workloads.config2(8192, batch=5), dev)
+    sorted_q["sorted"] = True
+    sorted_q["values"] = torch.empty((5, 1024), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def calls():
+        for w, q in zip(ws, probs):
+            if w.form == "paged":
+                pkg.topk_transform_paged(q["scores"], q["seq_lens"], q["page_table"], w.page_size,
+                                         w.k, out=q["out"], stream=stream)
+            elif w.form == "raw":
+                pkg.topk_transform_raw(q["scores"], q["seq_lens"], w.k, out=q["out"], stream=stream)
+            elif w.form == "ragged":
+                pkg.topk_transform_ragged(q["scores"], q["row_starts"], q["seq_lens"], w.k,
+                                          max_row_len_hint=q["max_row_len_hint"], out=q["out"],
+                                          stream=stream)
+            else:
+                pkg.topk_transform_window(q["scores"], q["starts"], q["seq_lens"], w.k,
+                                          max_row_len_hint=q["max_row_len_hint"], out=q["out"],
+                                          stream=stream)
+        pkg.topk_transform_grouped([sorted_q], stream=stream, static_workspace=True)
+
+    with torch.cuda.stream(stream):
+        calls()  # first calls set the device up outside the capture
+        stream.synchronize()
+        for q in probs + [sorted_q]:
+            q["out"].fill_(-7)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            calls()
+        for _ in range(3):
+            graph.replay()
+        stream.synchronize()
+    for w, q in zip(ws, probs):
+        assert_parity(w, q["out"].cpu().numpy())
+    w2 = workloads.config2(8192, batch=5)
+    assert_options(w2, sorted_q["out"].cpu().numpy(), sorted_q["values"].cpu().numpy(), True)
+
+
+def test_concurrent_streams(pkg):
+    """Two streams running different problems at the same time."""
+    dev = torch.device("cuda:0")
+    wa, wb = workloads.config3(128), many_rows("raw", 320, 7000, 900, 91)
+    qa, qb = problem_of(wa, dev), problem_of(wb, dev)
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        pkg.topk_transform_paged(qa["scores"], qa["seq_lens"], qa["page_table"], wa.page_size, wa.k,
+                                 out=qa["out"], stream=sa)
+        pkg.topk_transform_raw(qb["scores"], qb["seq_lens"], wb.k, out=qb["out"], stream=sb)
+    torch.cuda.synchronize()
+    assert_parity(wa, qa["out"].cpu().numpy())
+    assert_parity(wb, qb["out"].cpu().numpy())
