@@ -734,3 +734,59 @@ def test_concurrent_streams(pkg):
     torch.cuda.synchronize()
     assert_parity(wa, qa["out"].cpu().numpy())
     assert_parity(wb, qb["out"].cpu().numpy())
+
+
+# ------------------------------------------------------------ the filter-time L1 read-back
+# Single-CTA launches of more rows than SMs (152) with the 512-thread build read the
+# candidates' values back from L1 inside the filter.
+
+def special_rows(g, batch, stride):
+    """Rows mixing NaN of both signs, infinities, signed zeros, subnormals, exact
+    duplicates and ordinary values."""
+    x = workloads.random_rows(g, batch, stride, "normal", dup=True)
+    pick = g.random(x.shape)
+    x[pick < 0.01] = np.float32(np.nan)
+    x[(pick >= 0.01) & (pick < 0.02)] = -np.float32(np.nan)
+    x[(pick >= 0.02) & (pick < 0.03)] = np.float32(np.inf)
+    x[(pick >= 0.03) & (pick < 0.04)] = -np.float32(np.inf)
+    x[(pick >= 0.04) & (pick < 0.06)] = np.float32(0.0)
+    x[(pick >= 0.06) & (pick < 0.08)] = -np.float32(0.0)
+    x[(pick >= 0.08) & (pick < 0.10)] = np.float32(1e-40)
+    return x
+
+
+@pytest.mark.parametrize("stride", [3000, 20000])
+@pytest.mark.parametrize("form", ["raw", "paged", "ragged"])
+def test_keys_in_filter_special_values(pkg, stride, form):
+    """Short rows (every element a candidate, no sample) and sampled rows, with special
+    values, at a batch that takes the L1 read-back (and paged with a page size that
+    is not a power of two)."""
+    g = np.random.Generator(np.random.PCG64(stride + len(form)))
+    batch, k = 200, 1024
+    scores = special_rows(g, batch, stride)
+    seq = g.integers(0, stride + 5, size=batch).astype(np.int32)
+    seq[::3] = stride
+    if form == "raw":
+        w = workloads.Workload(f"keys_raw_{stride}", "raw", k, scores, seq)
+    elif form == "paged":
+        pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, 48))
+        w = workloads.Workload(f"keys_paged_{stride}", "paged", k, scores, seq, pt, 48)
+    else:
+        lens = np.minimum(seq, stride).astype(np.int64)
+        starts = np.concatenate([[7], 7 + np.cumsum(lens + 1)[:-1]]).astype(np.int32)
+        packed = np.zeros(int(starts[-1] + lens[-1] + 3), np.float32)
+        for b in range(batch):
+            packed[starts[b]:starts[b] + lens[b]] = scores[b, :lens[b]]
+        w = workloads.Workload(f"keys_ragged_{stride}", "ragged", k, packed,
+                               lens.astype(np.int32), None, 64, starts)
+    got = run_gpu(pkg, w)
+    exp = oracle.run(w)
+    assert same_sets(got, exp).all(), f"{w.name}: rows differ from the oracle"
+
+
+@pytest.mark.parametrize("tie_cap", [0, 300, 4096])
+def test_keys_in_filter_tie_capacity(pkg, tie_cap):
+    w = many_rows("paged", 200, 12000, 1024, 97 + tie_cap, "banded")
+    with settings(pkg, tie_cap=tie_cap):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
