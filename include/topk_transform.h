@@ -251,8 +251,9 @@ int topk_reset_guard_hits(void);
  * topk_set_cta_threads(t): which build of the kernels runs: 512-thread CTAs (two
  * per SM) or 256-thread CTAs (four per SM, at most 3072 tie-buffer entries); any
  * other value restores the built-in choice, which takes the 256-thread build for
- * launches of more rows than two CTAs per SM hold, rows of at most 8192 elements
- * (by row_stride, or the ragged hint), one CTA per row and k <= 1024.
+ * launches of more rows than two CTAs per SM hold, with one CTA per row, k <= 1024,
+ * and rows of at most 8192 elements (by row_stride, or the ragged and window hints)
+ * or at least 16 rows per SM.
  * The result is the same either way. */
 #define TOPK_TIE_CAPACITY_MAX 4096
 int topk_set_row_split(int g);

@@ -76,15 +76,18 @@ int choose_split(int64_t batch, int64_t row_len, int sm_count) {
 
 // Launches of more rows than two 512-thread CTAs per SM hold take the 256-thread
 // build (four CTAs per SM, so each SM overlaps more rows) when one CTA owns a row,
-// the rows are at most 8192 elements (measured: faster at 8192, slower at 16384
-// and 32768, where half the threads per row lengthen each row's chain more than
-// the extra rows hide) and every problem's candidates fit that build's smaller
-// buffer (k <= 1024). row_len <= 0 means unknown.
+// every problem's candidates fit that build's smaller buffer (k <= 1024), and
+// either the rows are at most 8192 elements or there are at least 16 rows per SM
+// (four waves of it). Measured: with shorter rows or enough waves the extra rows
+// in flight win; 1024 rows of 32768 (under two waves) run faster on the 512-thread
+// build, whose shorter per-row chain leaves a shorter last wave. row_len <= 0
+// means unknown.
 bool use_cta256(int64_t rows, int64_t row_len, int g, int32_t k_max, int sm_count) {
   const int forced = g_cta_threads.load(std::memory_order_relaxed);
   if (forced != 0) return forced == 256;
-  return g == 1 && rows > 2 * static_cast<int64_t>(sm_count) && k_max <= 1024 &&
-         row_len > 0 && row_len <= 8192;
+  const int64_t sms = sm_count;
+  return g == 1 && rows > 2 * sms && k_max <= 1024 &&
+         ((row_len > 0 && row_len <= 8192) || rows >= 16 * sms);
 }
 
 int fail_cuda(cudaError_t e) {
@@ -183,7 +186,8 @@ int run_one(const topk_problem_t& q, cudaStream_t stream) {
   cudaError_t e;
   if (use_cta256(p.batch, hint, g, p.k, ds->sm_count)) {
     p.tie_cap = std::min(p.tie_cap, topk_gb300::kTieCap256);
-    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, false, stream);
+    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, p.batch > ds->sm_count,
+                                   stream);
   } else {
     // more rows than SMs: SMs hold two CTAs and the candidates' L2 read-back
     // contends, so the filter reads them back from L1 instead (measured)
@@ -333,7 +337,8 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
     if (use_cta256(rows, hint, g, k_max, ds->sm_count)) {
       for (int i = 0; i < gp.n; ++i)
         gp.probs[i].tie_cap = std::min(gp.probs[i].tie_cap, topk_gb300::kTieCap256);
-      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts, false, stream);
+      e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts,
+                                           rows > ds->sm_count, stream);
     } else {
       e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, opts,
                                            rows > ds->sm_count, stream);
