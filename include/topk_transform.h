@@ -204,13 +204,35 @@ size_t topk_problem_workspace_bytes(const topk_problem_t* problems, int32_t n_pr
 int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* As topk_transform_grouped, with no workspace argument: sorted problems stage
- * their (key, position) pairs in a scratch array the library keeps in device
- * memory (a static __device__ array of TOPK_STATIC_WORKSPACE_BYTES per device, part
- * of the loaded module), so the call allocates nothing. Returns
- * TOPK_ERR_WORKSPACE_TOO_SMALL, before any launch, when the problems need more
- * than that (topk_problem_workspace_bytes). Calls that use the array must not
- * overlap on a device: issue them on one stream, or order their streams. */
+/* As topk_transform_grouped, with no workspace argument, for callers that cannot
+ * allocate device memory: a plug-in inside a host runtime that hands it only fixed
+ * input and output buffers and no allocator; a serving engine whose caching
+ * allocator has reserved the device's memory up front, so a cudaMalloc of its own
+ * would fail or stall every stream on an implicit synchronisation in the middle of
+ * a decode step. The pages have no counterpart: their exact kernel takes its
+ * workspace from PyTorch's allocator.
+ *
+ * Sorted problems stage their (key, position) pairs in a scratch array the library
+ * keeps in device memory instead: a static __device__ array of
+ * TOPK_STATIC_WORKSPACE_BYTES (16 MiB), part of the loaded module, so every device
+ * that loads the library holds it until the process exits. The call itself
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Limit: problems needing more than TOPK_STATIC_WORKSPACE_BYTES of staging
+ * (topk_problem_workspace_bytes: 8 bytes per output slot of each sorted problem,
+ * so more than 1024 rows at k = 2048) get TOPK_ERR_WORKSPACE_TOO_SMALL before any
+ * launch.
+ * Problems without TOPK_FLAG_SORTED never touch the array.
+ *
+ * Set-up: the first call on a device that has a sorted problem looks up the
+ * array's device address (cudaGetSymbolAddress, once per device, on the current
+ * device); make that first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last call's
+ * contents. Nothing in it needs to start at zero (the selection kernel writes every
+ * slot the sort pass reads, padding included). Calls whose launches overlap on the
+ * GPU race on the array and give wrong results: issue them on one stream, or order
+ * their streams. */
 #define TOPK_STATIC_WORKSPACE_BYTES (16u << 20)
 int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_problems,
                                   cudaStream_t stream);

@@ -256,8 +256,8 @@ class TopkProblem(ctypes.Structure):
 TOPK_FLAG_SORTED = 1
 
 
-def topk_transform_grouped(problems: list[dict], stream=None,
-                           static_workspace: bool = False) -> list[torch.Tensor]:
+def topk_transform_grouped(problems: list[dict], stream=None, static_workspace: bool = False,
+                           workspace: torch.Tensor | None = None) -> list[torch.Tensor]:
     """Several independent transforms in one call (one launch per form present).
 
     Each problem is a dict with "form" ("raw", "paged", "ragged" or "window"), "k",
@@ -267,9 +267,11 @@ def topk_transform_grouped(problems: list[dict], stream=None,
     [batch, k] fp32 device tensor that receives each slot's score (-inf in the
     padding slots), and "sorted": True for the slots in rank order (largest score
     first, equal scores by smaller position first). Sorted problems use a device
-    workspace this function allocates, or, with static_workspace=True, the
-    library's own scratch array (no allocation; such calls must not overlap on a
-    device). Returns the output tensors, in order."""
+    workspace: `workspace` (a uint8 device tensor of at least
+    topk_problem_workspace_bytes, owned by the caller), else one this function
+    allocates; or, with static_workspace=True, the library's own scratch array
+    (topk_transform_grouped_static: no allocation; such calls must not overlap on
+    a device). Returns the output tensors, in order."""
     lib = load_library()
     if len(problems) > TOPK_MAX_GROUP:
         raise ValueError(f"at most {TOPK_MAX_GROUP} problems per grouped call")
@@ -334,6 +336,16 @@ def topk_transform_grouped(problems: list[dict], stream=None,
         _check(st, "topk_transform_grouped_static")
         return outs
     ws_bytes = int(lib.topk_problem_workspace_bytes(ctypes.addressof(arr), len(problems)))
+    if workspace is not None:
+        _cuda_tensor(workspace, "workspace", torch.uint8, dev)
+        if not workspace.is_contiguous() or workspace.numel() < ws_bytes:
+            raise ValueError(f"workspace must be a contiguous uint8 tensor of at least {ws_bytes} bytes")
+        with torch.cuda.device(dev):
+            st = lib.topk_transform_grouped(ctypes.addressof(arr), len(problems),
+                                            workspace.data_ptr() if ws_bytes else None,
+                                            workspace.numel(), _stream(stream, dev))
+        _check(st, "topk_transform_grouped")
+        return outs
     with torch.cuda.device(dev):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
         st = lib.topk_transform_grouped(ctypes.addressof(arr), len(problems),

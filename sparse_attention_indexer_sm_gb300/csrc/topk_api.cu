@@ -25,6 +25,8 @@ std::atomic<int> g_fast_tier{1};
 std::atomic<int> g_cta_threads{0};  // 0: automatic; 512 or 256: that build
 
 // The scratch of topk_transform_grouped_static: part of the module, one per device.
+// Host code must not hand this name to a kernel: on the host it is only a stand-in
+// for the symbol; its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_static_stage[TOPK_STATIC_WORKSPACE_BYTES];
 thread_local int t_last_cuda_error = 0;
 
@@ -32,6 +34,9 @@ struct DeviceState {
   std::once_flag once;
   int sm_count = 0;
   cudaError_t err = cudaSuccess;
+  std::once_flag stage_once;      // the static scratch's device address, looked up once
+  void* stage = nullptr;
+  cudaError_t stage_err = cudaSuccess;
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -366,8 +371,13 @@ int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_prob
     DeviceState* ds = nullptr;  // loads the module on this device first
     const int st = device_state(&ds);
     if (st != TOPK_OK) return st;
-    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_static_stage);
-    if (e != cudaSuccess) return fail_cuda(e);
+    // Once per device, with that device current (device_state keyed the state by
+    // the current device): the array's device address.
+    std::call_once(ds->stage_once, [ds]() {
+      ds->stage_err = cudaGetSymbolAddress(&ds->stage, g_static_stage);
+    });
+    if (ds->stage_err != cudaSuccess) return fail_cuda(ds->stage_err);
+    scratch = ds->stage;
   }
   return topk_transform_grouped(problems, n_problems, scratch, need > 0 ? need : 0, stream);
 }

@@ -684,6 +684,7 @@ def test_calls_captured_in_a_cuda_graph(pkg):
     sorted_q = problem_of(workloads.config2(8192, batch=5), dev)
     sorted_q["sorted"] = True
     sorted_q["values"] = torch.empty((5, 1024), dtype=torch.float32, device=dev)
+    sort_ws = torch.empty(5 * 1024 * 8, dtype=torch.uint8, device=dev)  # allocated before capture
     stream = torch.cuda.Stream(dev)
 
     def calls():
@@ -701,7 +702,7 @@ def test_calls_captured_in_a_cuda_graph(pkg):
                 pkg.topk_transform_window(q["scores"], q["starts"], q["seq_lens"], w.k,
                                           max_row_len_hint=q["max_row_len_hint"], out=q["out"],
                                           stream=stream)
-        pkg.topk_transform_grouped([sorted_q], stream=stream, static_workspace=True)
+        pkg.topk_transform_grouped([sorted_q], stream=stream, workspace=sort_ws)
 
     with torch.cuda.stream(stream):
         calls()  # first calls set the device up outside the capture
