@@ -696,9 +696,10 @@ __device__ __forceinline__ void merge_into_cta0(const uint32_t* h, uint32_t* mh,
 // the header comment). The kH1 and kH2 regions of `hist` and of CTA 0's `mhist`
 // are zero on entry, and so is CTA 0's ctl.ns. Returns lambda; *shift2 gets the
 // candidate-histogram bin width exponent.
-__device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice& s, int32_t L,
-                                                  uint32_t k, int G, int rank, uint32_t* hist,
-                                                  uint32_t* mhist, Ctl& ctl, uint32_t* shift2) {
+__device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice& s, bool prefetched,
+                                                  int32_t L, uint32_t k, int G, int rank,
+                                                  uint32_t* hist, uint32_t* mhist, Ctl& ctl,
+                                                  uint32_t* shift2) {
   const int tid = threadIdx.x;
   const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
   // round 1: coarse bins (top 10 key bits), one shared atomic per sample key (this
@@ -724,7 +725,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   if (G > 1) merge_into_cta0(hist + kH1, mhist + kH1, kFastWords);
   // the sample has arrived: now the bulk of the slice, issued by the last warp while
   // the first one looks for the thresholds
-  prefetch_slice(s, kThreads - 32);
+  if (!prefetched) prefetch_slice(s, kThreads - 32);
   // sample ranks a few standard deviations either side of the expected sample rank
   // of the row's k-th key
   uint32_t rs = 0, rs_lo = 0;
@@ -1347,9 +1348,11 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   bool sample_loaded = false;
   if constexpr (form_of(F) == kRaw || form_of(F) == kPaged) {
     if (p.use_filter && p.row_stride > static_cast<int64_t>(p.tie_cap) && p.row_stride <= INT32_MAX) {
-      load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
-                             static_cast<int32_t>(p.row_stride), rank, G),
-                  sm);
+      const Slice whole = make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
+                                     static_cast<int32_t>(p.row_stride), rank, G);
+      load_sample(whole, sm);
+      // right behind the sample: the whole stride towards L2 (from the last warp)
+      prefetch_slice(whole, kThreads - 32);
       sample_loaded = true;
     }
   }
@@ -1426,7 +1429,8 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   if (p.use_filter) {
     uint32_t shift2 = 32 - kFastBits;  // rows that skip the sample: the top key bits
     const uint32_t lambda =
-        sampled ? sample_lambda(sm, s, L, static_cast<uint32_t>(k), G, rank, hist, mhist, ctl, &shift2)
+        sampled ? sample_lambda(sm, s, sample_loaded, L, static_cast<uint32_t>(k), G, rank, hist,
+                                mhist, ctl, &shift2)
                 : 0u;
     if constexpr (form_of(F) == kPaged) {
       if (pages > 0) {
