@@ -94,7 +94,7 @@ constexpr uint32_t kPrefetchBytes = 16384;  // one bulk L2 prefetch
 // from global memory); the 256-thread build keeps its shared memory within a
 // quarter of the SM's
 constexpr int kPtCap = kThreads == 512 ? 4096 : 1024;
-constexpr int kRankDirect = 64;       // threshold bins this small are ordered by rank count
+constexpr int kRankDirect = 128;      // threshold bins this small are ordered by rank count
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Histograms are stored padded, one spare word after every 32 bins, so that the
@@ -118,7 +118,12 @@ constexpr int kFastWords = hist_index(kFastBins);
 constexpr int kH1 = 0;                // sample, coarse round
 constexpr int kH2 = kFastWords;       // sample, fine round
 constexpr int kHC = 2 * kFastWords;   // candidates
-static_assert(3 * kFastWords <= kHistWords, "fast-tier histograms must fit the histogram region");
+// The candidate histogram has 2048 bins (its region runs to the end of `hist`): the
+// finer its bins, the fewer candidates share the threshold bin.
+constexpr int kCandBits = 11;
+constexpr int kCandBins = 1 << kCandBits;
+constexpr int kCandWords = hist_index(kCandBins);
+static_assert(kHC + kCandWords <= kHistWords, "fast-tier histograms must fit the histogram region");
 
 struct Ctl {
   uint32_t scan[kWarps];              // per-warp partials of block scans
@@ -428,6 +433,58 @@ __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, ui
     ctl.sel2_t = static_cast<uint32_t>(b2);
     ctl.sel2_above = a2;
     ctl.sel2_count = c2;
+  }
+}
+
+// One warp (all 32 lanes) finds, in the padded kCandBins-bin candidate histogram h,
+// the bin where the count from the top reaches need (1 <= need <= sum of h) and
+// writes it to ctl.sel_* (visible to the block after the caller's next barrier):
+// lane l sums bins [P l, P l + P) (P = kCandBins / 32); a suffix scan over the lanes
+// names the owner of the threshold; then each lane takes P / 32 of the owner's bins.
+__device__ __forceinline__ void warp_find_cand(const uint32_t* h, uint32_t need, Ctl& ctl) {
+  constexpr int P = kCandBins / 32;  // bins per lane in the first step
+  constexpr int P2 = P / 32;         // bins per lane in the second step
+  const int lane = threadIdx.x & 31;
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < P; ++i) s += h[hist_index(lane * P + i)];
+  uint32_t x = s;  // count in the bins of lanes >= lane
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_down_sync(kFull, x, off);
+    if (lane + off < 32) x += y;
+  }
+  const uint32_t hit = __ballot_sync(kFull, s != 0 && x - s < need && need <= x);
+  if (hit == 0u) return;  // need outside [1, sum]: nothing to find
+  const int o = __ffs(hit) - 1;
+  const uint32_t above = __shfl_sync(kFull, x - s, o);
+  const int b0 = o * P + lane * P2;  // this lane's bins [b0, b0 + P2) of the owner's range
+  uint32_t c[P2];
+  uint32_t s2 = 0;
+#pragma unroll
+  for (int i = 0; i < P2; ++i) {
+    c[i] = h[hist_index(b0 + i)];
+    s2 += c[i];
+  }
+  uint32_t y = s2;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t z = __shfl_down_sync(kFull, y, off);
+    if (lane + off < 32) y += z;
+  }
+  uint32_t acc = above + y - s2;  // count above this lane's bins
+  const uint32_t here = __ballot_sync(kFull, s2 != 0 && acc < need && need <= acc + s2);
+  if (here != 0u && lane == __ffs(here) - 1) {
+#pragma unroll
+    for (int i = P2 - 1; i >= 0; --i) {
+      if (acc + c[i] >= need) {
+        ctl.sel_t = static_cast<uint32_t>(b0 + i);
+        ctl.sel_above = acc;
+        ctl.sel_count = c[i];
+        break;
+      }
+      acc += c[i];
+    }
   }
 }
 
@@ -803,10 +860,10 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
         const uint64_t gap = hi > lam ? hi - lam : 0;
         const int bits = 64 - __clzll(static_cast<long long>(gap));
         ctl.lambda = lam;
-        ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - (kFastBits - 1)));
+        ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - (kCandBits - 1)));
       } else {
         ctl.lambda = 0;
-        ctl.lambda_shift = 32 - kFastBits;
+        ctl.lambda_shift = 32 - kCandBits;
       }
     }
     __syncwarp();
@@ -843,7 +900,7 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
 // afterwards); with kKeys the loads keep their lines in L1, the masks are decoded
 // every iteration (MI = 1) and each candidate's value is read back from L1 at
 // once: the entry gets its key and the candidate histogram `chist` (bin =
-// min((key - lambda) >> shift, kFastBins - 1); zero on entry) its count. Slots at
+// min((key - lambda) >> shift, kCandBins - 1); zero on entry) its count. Slots at
 // or beyond `cap` are counted but not written.
 template <bool kPos, bool kKeys>
 __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint32_t shift,
@@ -893,7 +950,7 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
         if constexpr (kKeys) {
           const uint32_t key = order_key(__float_as_uint(__ldg(s.row + j)));  // from L1
           const uint32_t d = (key - lambda) >> shift;
-          if (d >= static_cast<uint32_t>(kFastBins - 1))
+          if (d >= static_cast<uint32_t>(kCandBins - 1))
             ++top;
           else
             atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
@@ -920,13 +977,13 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
   if constexpr (kKeys) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
-    if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kFastBins - 1)], top);
+    if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
   }
 }
 
 // F2, a row owned by one CTA: the n buffered positions get their keys, read back
 // (from L2) in batches of 2048, and the candidate histogram (bin =
-// min((key - lambda) >> shift, kFastBins - 1)) is counted in `chist`, which is zero
+// min((key - lambda) >> shift, kCandBins - 1)) is counted in `chist`, which is zero
 // on entry. The last
 // bin collects most candidates, so it is counted per warp (ballot) rather than by
 // one shared atomic per candidate.
@@ -951,14 +1008,14 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
       const uint32_t i = i0 + r * kThreads;
       const uint32_t key = order_key(bits[r]);
       const uint32_t d = (key - lambda) >> shift;
-      const bool top = i < n && d >= static_cast<uint32_t>(kFastBins - 1);
+      const bool top = i < n && d >= static_cast<uint32_t>(kCandBins - 1);
       if (i < n) {
         buf[i].x = key;
         if (!top) atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
       }
       const uint32_t b = __ballot_sync(kFull, top);
       if ((tid & 31) == 0 && b != 0)
-        atomicAdd(&chist[hist_index(kFastBins - 1)], static_cast<uint32_t>(__popc(b)));
+        atomicAdd(&chist[hist_index(kCandBins - 1)], static_cast<uint32_t>(__popc(b)));
     }
   }
   __syncthreads();
@@ -966,7 +1023,7 @@ __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, ui
 
 // F2, a row split over a cluster: stream the slice; every element with key >=
 // lambda goes, as (key, position), to CTA 0's buffer and into this CTA's candidate
-// histogram `chist` (bin = min((key - lambda) >> shift, kFastBins - 1); zero on
+// histogram `chist` (bin = min((key - lambda) >> shift, kCandBins - 1); zero on
 // entry), so
 // that CTA 0 does not have to read the keys back for the whole row. Slots come
 // from one reservation per warp and iteration on CTA 0's counter through
@@ -986,7 +1043,7 @@ __device__ __forceinline__ void filter_candidates(const Slice& s, uint32_t lambd
   auto put = [&](uint32_t slot, uint32_t bits, int32_t j) {
     const uint32_t key = order_key(bits);
     const uint32_t d = (key - lambda) >> shift;
-    if (d >= static_cast<uint32_t>(kFastBins - 1))
+    if (d >= static_cast<uint32_t>(kCandBins - 1))
       ++top;
     else
       atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
@@ -1037,7 +1094,7 @@ __device__ __forceinline__ void filter_candidates(const Slice& s, uint32_t lambd
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
-  if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kFastBins - 1)], top);
+  if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
 }
 
 // ------------------------------------------------------------------ selection in a buffer
@@ -1112,7 +1169,7 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
 }
 
 // F3 (CTA 0 only): the filter left n candidates in buf and their histogram (bin =
-// min((key - lambda) >> shift, kFastBins - 1)) in chist. Writes the k largest composites
+// min((key - lambda) >> shift, kCandBins - 1)) in chist. Writes the k largest composites
 // (key, ~position) mapped to out. h may be chist itself: it is used only after
 // chist has been read.
 template <int F>
@@ -1122,7 +1179,7 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
                                                   int32_t L, int32_t* out, const OutMap& m,
                                                   Ctl& ctl) {
   const int tid = threadIdx.x;
-  if (tid < 32) warp_find2(chist, k, 0u, false, ctl);
+  if (tid < 32) warp_find_cand(chist, k, ctl);
   __syncthreads();
   const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
   if (ct > static_cast<uint32_t>(kListCap)) {
@@ -1139,7 +1196,7 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
   for (int r = 0; r < kPer; ++r) {
     const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
     if (i < n) {
-      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kFastBins - 1));
+      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kCandBins - 1));
       if (b > t) {
         cls |= 1u << (2 * r);
         ++nw;
@@ -1173,18 +1230,56 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
   }
   __syncthreads();
   const uint32_t need = k - above;  // 1 <= need <= ct
-  if (ct <= static_cast<uint32_t>(kRankDirect)) {
-    // order the bin by counting: entry i takes slot above + (#entries ranked before it)
+  // entry o ranks before entry e: a larger key, or an equal key at a smaller position
+  auto before = [](uint2 e, uint32_t ox, uint32_t oy) -> uint32_t {
+    return static_cast<uint32_t>(ox > e.x) |
+           (static_cast<uint32_t>(ox == e.x) & static_cast<uint32_t>(oy < e.y));
+  };
+  if (ct <= 32u) {  // order the bin by counting, one thread per entry
     if (static_cast<uint32_t>(tid) < ct) {
       const uint2 e = list[tid];
-      const uint64_t v = (static_cast<uint64_t>(e.x) << 32) | static_cast<uint64_t>(~e.y);
       uint32_t r = 0;
       for (uint32_t j = 0; j < ct; ++j) {
         const uint2 o = list[j];
-        const uint64_t w = (static_cast<uint64_t>(o.x) << 32) | static_cast<uint64_t>(~o.y);
-        r += w > v ? 1u : 0u;
+        r += before(e, o.x, o.y);
       }
       if (r < need) emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y), e.x);
+    }
+    return;
+  }
+  if (ct <= static_cast<uint32_t>(kRankDirect)) {
+    // order the bin by counting: entry i takes slot above + (#entries ranked before
+    // it). Each entry gets a group of g consecutive lanes (g a power of two, g * ct
+    // <= kThreads, g <= ct and at most a warp) that split the comparisons and add
+    // them up.
+    int g = 32;
+    while (g > 1 && (static_cast<uint32_t>(g) * ct > static_cast<uint32_t>(kThreads) ||
+                     static_cast<uint32_t>(g) > ct))
+      g >>= 1;
+    const uint32_t i = static_cast<uint32_t>(tid) / static_cast<uint32_t>(g);
+    const uint32_t part = static_cast<uint32_t>(tid) & static_cast<uint32_t>(g - 1);
+    // the whole warp takes part in the shuffles; lanes past the last entry count nothing
+    const bool live = i < ct;
+    uint2 e = make_uint2(0u, 0u);
+    uint32_t r = 0;
+    if (live) {
+      e = list[i];
+      // two entries per 16-byte load: pairs (2q, 2q + 1), q = part, part + g, ...
+      const uint4* pairs = reinterpret_cast<const uint4*>(list);
+      const uint32_t npairs = ct >> 1;
+      for (uint32_t q = part; q < npairs; q += static_cast<uint32_t>(g)) {
+        const uint4 o = pairs[q];
+        r += before(e, o.x, o.y) + before(e, o.z, o.w);
+      }
+      if ((ct & 1u) != 0u && part == static_cast<uint32_t>(g - 1)) {
+        const uint2 o = list[ct - 1];
+        r += before(e, o.x, o.y);
+      }
+    }
+    if (tid < ((static_cast<int>(ct) * g + 31) & ~31)) {  // whole warps that hold an entry
+      for (int off = g >> 1; off > 0; off >>= 1) r += __shfl_xor_sync(kFull, r, off);
+      if (live && part == 0u && r < need)
+        emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y), e.x);
     }
     return;
   }
@@ -1427,7 +1522,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
 
   // ---------------- fast tier
   if (p.use_filter) {
-    uint32_t shift2 = 32 - kFastBits;  // rows that skip the sample: the top key bits
+    uint32_t shift2 = 32 - kCandBits;  // rows that skip the sample: the top key bits
     const uint32_t lambda =
         sampled ? sample_lambda(sm, s, sample_loaded, L, static_cast<uint32_t>(k), G, rank, hist,
                                 mhist, ctl, &shift2)
@@ -1462,7 +1557,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
                                  chist, ctl);
       cluster_sync();  // every candidate is in CTA 0's buffer; the counter is final
       if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
-      merge_into_cta0(chist, mhist + kHC, kFastWords);  // ends with a cluster barrier
+      merge_into_cta0(chist, mhist + kHC, kCandWords);  // ends with a cluster barrier
       n_cand = ctl.n_cand;
       chist = mhist + kHC;
     }

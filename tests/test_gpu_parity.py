@@ -791,3 +791,37 @@ def test_keys_in_filter_tie_capacity(pkg, tie_cap):
     with settings(pkg, tie_cap=tie_cap):
         got = run_gpu(pkg, w)
     assert_parity(w, got)
+
+
+# ------------------------------------------------------------ threshold-bin sizes
+# The candidates of the threshold bin are ordered by a direct rank count up to the
+# CTA size and by radix rounds beyond it.
+
+def threshold_bin_rows(batch, stride, k, dup, seed):
+    """Rows whose k-th score is repeated `dup` times (the repeats straddle rank k),
+    so the threshold bin holds at least `dup` equal keys; some rows centre the
+    scores near zero, where the key jumps across the sign."""
+    g = workloads.rng(seed)
+    scores = workloads.random_rows(g, batch, stride, "normal")
+    for b in range(batch):
+        row = scores[b]
+        if b % 2 == 1:
+            row -= np.float32(1.86)  # the k-th score near zero
+        order = np.argsort(-row, kind="stable")
+        v = row[order[k - 1 - dup // 2]]
+        pos = g.choice(stride, size=dup, replace=False)
+        row[pos] = v
+    return scores
+
+
+@pytest.mark.parametrize("cta", [512, 256])
+@pytest.mark.parametrize("dup", [1, 2, 3, 63, 64, 65, 127, 128, 129, 200, 256, 257, 512, 513, 900])
+def test_threshold_bin_sizes(pkg, dup, cta):
+    batch, stride, k = 6, 32768, 1024
+    scores = threshold_bin_rows(batch, stride, k, dup, 1300 + dup)
+    seq = np.full(batch, stride, np.int32)
+    w = workloads.Workload(f"tbin_{dup}", "raw", k, scores, seq)
+    with settings(pkg, cta=cta, split=1):
+        assert_parity(w, run_gpu(pkg, w))
+    with settings(pkg, cta=cta, split=4):
+        assert_parity(w, run_gpu(pkg, w))
