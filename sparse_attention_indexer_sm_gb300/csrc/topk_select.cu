@@ -24,10 +24,10 @@
 //                pattern with lambda (a single integer compare: for lambda in the
 //                non-negative range a signed compare, otherwise an unsigned one,
 //                both equal to "key >= lambda"). Candidates go to CTA 0's shared
-//                buffer as (key, position) and are counted in a 1024-bin candidate
+//                buffer as (key, position) and are counted in a 2048-bin candidate
 //                histogram whose bins of width 2^s2 start at lambda (s2 chosen so that
-//                fewer than 512 bins span [lambda, lambda_hi]; the last bin takes
-//                every larger key; rows that skip the sample use the top 10 key bits).
+//                fewer than 1024 bins span [lambda, lambda_hi]; the last bin takes
+//                every larger key; rows that skip the sample use the top 11 key bits).
 //                A row owned by one CTA keeps only positions in the pass (so the
 //                loads of several iterations stay in flight) and reads the candidates'
 //                values back from L2 afterwards; the CTAs of a cluster write keys and
@@ -36,9 +36,10 @@
 //                element of the exact top-k is among them (they hold k elements with
 //                key >= lambda, so the k-th key is >= lambda). CTA 0 finds the
 //                threshold bin of the candidate histogram, writes the candidates above
-//                it, and orders the few candidates of that bin on the 64-bit composite
-//                (key, ~position), so equal keys go to the smaller position. Otherwise
-//                the exact tier runs.
+//                it, and orders the candidates of that bin on the 64-bit composite
+//                (key, ~position), so equal keys go to the smaller position: by a rank
+//                count spread over the CTA up to 128 of them, by radix rounds beyond.
+//                Otherwise the exact tier runs.
 //
 // Exact tier (any distribution; the page's design, re-planned):
 //  E1. rounds    4096-bin shared histograms of the top 12 key bits over the slice
@@ -853,7 +854,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
     __syncwarp();
     if (tid == 0) {
       if (rs != 0) {
-        // [lambda, lambda_hi] spans fewer than 512 candidate bins
+        // [lambda, lambda_hi] spans fewer than 1024 candidate bins
         const uint32_t lam = win_lo + (ctl.sel_t << f);
         const uint64_t hi =
             static_cast<uint64_t>(win_lo) + (static_cast<uint64_t>(ctl.sel2_t + 1) << f) - 1;
