@@ -38,7 +38,7 @@
 //                threshold bin of the candidate histogram, writes the candidates above
 //                it, and orders the candidates of that bin on the 64-bit composite
 //                (key, ~position), so equal keys go to the smaller position: by a rank
-//                count spread over the CTA up to 128 of them, by radix rounds beyond.
+//                count spread over the CTA up to 256 of them, by radix rounds beyond.
 //                Otherwise the exact tier runs.
 //
 // Exact tier (any distribution; the page's design, re-planned):
@@ -95,7 +95,7 @@ constexpr uint32_t kPrefetchBytes = 16384;  // one bulk L2 prefetch
 // from global memory); the 256-thread build keeps its shared memory within a
 // quarter of the SM's
 constexpr int kPtCap = kThreads == 512 ? 4096 : 1024;
-constexpr int kRankDirect = 128;      // threshold bins this small are ordered by rank count
+constexpr int kRankDirect = 256;      // threshold bins this small are ordered by rank count
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Histograms are stored padded, one spare word after every 32 bins, so that the
