@@ -370,9 +370,23 @@ def cpu_baseline(w, seconds: float = 1.5):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
+    # the same oracle on one core, over the workload's first 32 rows at a time
+    n1 = min(32, w.batch)
+    part = workloads.Workload(w.name, w.form, w.k, w.scores[:n1], w.seq_lens[:n1],
+                              w.page_table[:n1] if w.page_table is not None else None, w.page_size)
+    rows1, t1 = 0, time.perf_counter()
+    while True:
+        o.run(part, threads=1)
+        rows1 += n1
+        el1 = time.perf_counter() - t1
+        if el1 >= seconds / 3:
+            break
     return {"value": rows / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows} rows ({rows // w.batch} full batches of the bench workload), "
-                      f"{el:.2f} s wall on {cores} threads"}
+                      f"{el:.2f} s wall on {cores} threads",
+            "single_core_value": rows1 / el1,
+            "single_core_sample": f"{rows1} rows ({n1} rows of the bench workload at a time), "
+                                  f"{el1:.2f} s wall on 1 thread"}
 
 
 def workload_for(batch: int, form: str):
