@@ -357,6 +357,32 @@ def time_e2e(pkg, w, steps, dev, torch):
     return secs, h2d, d2h
 
 
+def single_call_latency(pkg, dev, torch, calls: int = 200):
+    """One paged call at B=1 (c4_len=32768, k=1024) at a time, the stream idle
+    before each: the median device time between events around the call, and the
+    median host wall time from the call to its completion (launch included)."""
+    w = workload_for(1, "paged")
+    sets = device_sets(w, 2, dev, torch)
+    stream = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dev_us, wall_us = [], []
+    with torch.cuda.stream(stream):
+        for i in range(calls + 10):
+            stream.synchronize()
+            t0 = time.perf_counter()
+            e0.record(stream)
+            call(pkg, w, sets[i % 2], stream)
+            e1.record(stream)
+            stream.synchronize()
+            t1 = time.perf_counter()
+            if i >= 10:  # warm-up calls first
+                dev_us.append(e0.elapsed_time(e1) * 1e3)
+                wall_us.append((t1 - t0) * 1e6)
+    return {"batch": 1, "form": "paged", "workload": "B=1 single call (stream idle before it)",
+            "device_us_median": statistics.median(dev_us), "wall_us_median": statistics.median(wall_us),
+            "calls": calls}
+
+
 def cpu_baseline(w, seconds: float = 1.5):
     """The oracle as it stands, on every host core, over whole batches of the same
     workload until about `seconds` of wall time (a bounded sample)."""
@@ -521,6 +547,21 @@ def run_ours(args):
         sweep.append({"batch": 256, "form": "grouped", "workload": "4 x paged B=64 c4_len=32768 k=1024",
                       "us_per_call": tg * 1e6, "us_per_call_separate": tsep * 1e6,
                       "gbs": ab / tg / 1e9, "frac": ab / tg / 1e9 / peak})
+        # the headline workload with its inputs hot in L2 (two input sets replayed), and
+        # the latency of one call at B=1 issued by itself; labelled extras, never the
+        # headline (a failure here leaves the line intact)
+        try:
+            s, _, _, ns = time_steps(pkg, w, 20000, 20, dev, torch, 0)
+            pc = s / 20000
+            sweep.append({"batch": w.batch, "form": w.form, "workload": "headline, L2-hot",
+                          "l2": f"hot: {ns} input sets ({ns * w.scores.nbytes / 1e6:.0f} MB) replayed",
+                          "us_per_call": pc * 1e6, "gbs": alg / pc / 1e9, "frac": alg / pc / 1e9 / peak})
+        except Exception as exc:  # noqa: BLE001
+            sweep.append({"workload": "headline, L2-hot", "error": repr(exc)})
+        try:
+            sweep.append(single_call_latency(pkg, dev, torch))
+        except Exception as exc:  # noqa: BLE001
+            sweep.append({"workload": "B=1 single call", "error": repr(exc)})
         result["sweep"] = sweep
     if rank == 0:
         print(json.dumps(result), flush=True)
