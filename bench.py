@@ -47,6 +47,7 @@ KERNEL_NAME = "topk_rows_kernel"
 KERNEL_SRC = os.path.join(ROOT, "sparse_attention_indexer_sm_gb300", "csrc", "topk_select.cu")
 PROFILE = os.path.join(ROOT, "profiles", "topk_rows_kernel_paged_b256_n32768.md")
 L2_FACTOR = 4
+REFERENCE_BUDGET_S = 120.0  # the reference arm's timed steps fit about this many seconds
 
 
 def parse_args():
@@ -579,18 +580,28 @@ def run_reference(args):
     o = oracle.default()
     cores = o.usable_cores()
     w = workload_for(args.batch, args.form)
-    # one step: `cores` rows of the workload, one per host core
+
+    def part(n):
+        return workloads.Workload(w.name, w.form, w.k, w.scores[:n], w.seq_lens[:n],
+                                  None if w.page_table is None else w.page_table[:n], w.page_size)
+
+    # one step: `rows_per_step` rows of the workload, one per thread (all host cores);
+    # the warm-up steps time a step, and the sample shrinks (down to one row on one
+    # thread) until the K timed steps fit REFERENCE_BUDGET_S
     rows_per_step = min(cores, w.batch)
-    sub = workloads.Workload(w.name, w.form, w.k, w.scores[:rows_per_step],
-                             w.seq_lens[:rows_per_step],
-                             None if w.page_table is None else w.page_table[:rows_per_step],
-                             w.page_size)
-    for _ in range(args.warmup):
-        o.run(sub, threads=cores)
+    sub = part(rows_per_step)
+    for i in range(max(args.warmup, 1)):
+        t = time.perf_counter()
+        o.run(sub, threads=rows_per_step)
+        step = time.perf_counter() - t
+        if args.steps * step > REFERENCE_BUDGET_S and rows_per_step > 1:
+            rows_per_step = max(1, int(rows_per_step * REFERENCE_BUDGET_S / (args.steps * step)))
+            sub = part(rows_per_step)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        o.run(sub, threads=cores)
+        o.run(sub, threads=rows_per_step)
     secs = time.perf_counter() - t0
+    cores = rows_per_step
     value = rows_per_step * args.steps / secs
     print(json.dumps({
         "impl": "reference",
@@ -601,7 +612,7 @@ def run_reference(args):
         "config": {"workload": describe(w), "batch_per_gpu": w.batch, "c4_len": C4_LEN, "k": w.k,
                    "form": w.form, "page_size": w.page_size},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {rows_per_step} rows of the workload, one per core"},
+                         "sample": f"each step: {rows_per_step} rows of the workload, one per thread"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
