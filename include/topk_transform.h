@@ -55,8 +55,12 @@
  *               scores + b * row_stride + lo. Any alignment of a row start is
  *               accepted.
  *   seq_lens    [batch]
- *   page_table  [batch, page_table_stride]; entries are trusted: the entries for
- *               pages 0 .. ceil(L/page_size)-1 of each row must exist.
+ *   page_table  [batch, page_table_stride]; entries are trusted. Each row must
+ *               hold the entries of pages 0 .. ceil(L/page_size)-1, so
+ *               page_table_stride >= ceil(L/page_size) for every row. A row that
+ *               needs more pages than page_table_stride never reads past its own
+ *               entries: the kernel counts it once in topk_guard_hits and writes
+ *               -1 for each selected position whose page is missing.
  *   row_starts  [batch], element offsets into `scores`; row_starts[b] + j must
  *               fit in int32.
  *   starts      [batch] (window form), any int32 value: it is clamped as above.
@@ -107,7 +111,8 @@ int topk_transform_raw(const float* scores, int64_t row_stride, const int32_t* s
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Paged form: as raw, each position mapped through the row's page table
- * (page_size >= 1, page_table_stride >= 1). */
+ * (page_size >= 1; page_table_stride >= 1, and at least ceil(L/page_size) for
+ * every row, see page_table above). */
 int topk_transform_paged(const float* scores, int64_t row_stride, const int32_t* seq_lens,
                          const int32_t* page_table, int64_t page_table_stride,
                          int32_t page_size, int32_t batch, int32_t k, int32_t* out,
@@ -209,8 +214,7 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
  * input and output buffers and no allocator; a serving engine whose caching
  * allocator has reserved the device's memory up front, so a cudaMalloc of its own
  * would fail or stall every stream on an implicit synchronisation in the middle of
- * a decode step. The pages have no counterpart: their exact kernel takes its
- * workspace from PyTorch's allocator.
+ * a decode step.
  *
  * Sorted problems stage their (key, position) pairs in a scratch array the library
  * keeps in device memory instead: a static __device__ array of

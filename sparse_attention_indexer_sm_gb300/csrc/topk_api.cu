@@ -34,9 +34,10 @@ struct DeviceState {
   std::once_flag once;
   int sm_count = 0;
   cudaError_t err = cudaSuccess;
-  std::once_flag stage_once;      // the static scratch's device address, looked up once
-  void* stage = nullptr;
-  cudaError_t stage_err = cudaSuccess;
+  // The static scratch's device address, stored once a lookup has succeeded (a
+  // failed lookup is not remembered: the next call tries again).
+  std::mutex stage_mu;
+  std::atomic<void*> stage{nullptr};
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -216,6 +217,22 @@ size_t staging_bytes(const topk_problem_t* problems, int32_t n, size_t* offsets)
   return total;
 }
 
+// The checks of a grouped call, in order: the array, then each problem. Fills the
+// problems' kernel parameters, row-length hints and the rows of each form.
+int check_group(const topk_problem_t* problems, int32_t n_problems, Params* params,
+                int64_t* hints, int64_t* rows_of_form) {
+  static_assert(TOPK_MAX_GROUP <= topk_gb300::kMaxGroup, "group limit");
+  if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
+  if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n_problems; ++i) {
+    hints[i] = 0;
+    const int st = build_params(problems[i], &params[i], &hints[i]);
+    if (st != TOPK_OK) return st;
+    rows_of_form[problems[i].form] += problems[i].batch;
+  }
+  return TOPK_OK;
+}
+
 topk_problem_t problem(int32_t form, const float* scores, int64_t row_stride,
                        const int32_t* seq_lens, int32_t batch, int32_t k, int32_t* out) {
   topk_problem_t q = {};
@@ -283,19 +300,12 @@ int topk_transform_window(const float* scores, int64_t row_stride, const int32_t
 
 int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
-  if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
   // every problem is checked before anything is launched
-  static_assert(TOPK_MAX_GROUP <= topk_gb300::kMaxGroup, "group limit");
   Params params[TOPK_MAX_GROUP];
   int64_t hints[TOPK_MAX_GROUP];
   int64_t rows_of_form[4] = {0, 0, 0, 0};
-  for (int i = 0; i < n_problems; ++i) {
-    hints[i] = 0;
-    const int st = build_params(problems[i], &params[i], &hints[i]);
-    if (st != TOPK_OK) return st;
-    rows_of_form[problems[i].form] += problems[i].batch;
-  }
+  const int checked = check_group(problems, n_problems, params, hints, rows_of_form);
+  if (checked != TOPK_OK) return checked;
   // sorted problems stage (key, position) pairs in the workspace
   size_t offsets[TOPK_MAX_GROUP];
   const size_t need = staging_bytes(problems, n_problems, offsets);
@@ -362,8 +372,13 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
 
 int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_problems,
                                   cudaStream_t stream) {
-  if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
-  if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
+  {  // every problem first, as the workspace call does, then the array's limit
+    Params params[TOPK_MAX_GROUP];
+    int64_t hints[TOPK_MAX_GROUP];
+    int64_t rows_of_form[4] = {0, 0, 0, 0};
+    const int checked = check_group(problems, n_problems, params, hints, rows_of_form);
+    if (checked != TOPK_OK) return checked;
+  }
   const size_t need = staging_bytes(problems, n_problems, nullptr);
   if (need > TOPK_STATIC_WORKSPACE_BYTES) return TOPK_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
@@ -371,13 +386,18 @@ int topk_transform_grouped_static(const topk_problem_t* problems, int32_t n_prob
     DeviceState* ds = nullptr;  // loads the module on this device first
     const int st = device_state(&ds);
     if (st != TOPK_OK) return st;
-    // Once per device, with that device current (device_state keyed the state by
-    // the current device): the array's device address.
-    std::call_once(ds->stage_once, [ds]() {
-      ds->stage_err = cudaGetSymbolAddress(&ds->stage, g_static_stage);
-    });
-    if (ds->stage_err != cudaSuccess) return fail_cuda(ds->stage_err);
-    scratch = ds->stage;
+    // The array's device address, looked up with its device current (device_state
+    // keyed the state by the current device) and kept only once the lookup worked.
+    scratch = ds->stage.load(std::memory_order_acquire);
+    if (scratch == nullptr) {
+      std::lock_guard<std::mutex> lock(ds->stage_mu);
+      scratch = ds->stage.load(std::memory_order_acquire);
+      if (scratch == nullptr) {
+        const cudaError_t e = cudaGetSymbolAddress(&scratch, g_static_stage);
+        if (e != cudaSuccess) return fail_cuda(e);
+        ds->stage.store(scratch, std::memory_order_release);
+      }
+    }
   }
   return topk_transform_grouped(problems, n_problems, scratch, need > 0 ? need : 0, stream);
 }

@@ -628,6 +628,8 @@ __device__ __forceinline__ void prefetch_slice(const Slice& s, int first = 0) {
 struct OutMap {
   const int32_t* pt_row;  // paged: this row's page table (global memory)
   const int32_t* pt_smem; // paged: the same entries staged in shared memory, or null
+  int32_t pt_n;           // paged: entries of the row that may be read (the row's pages,
+                          // at most the table's row stride)
   int32_t ps;             // page size
   int32_t ps_shift;       // log2(ps) or -1
   int32_t rstart;         // ragged: row start in the packed buffer; window: its first column
@@ -662,6 +664,9 @@ __device__ __forceinline__ int32_t map_pos(const OutMap& m, int32_t j) {
       page = j / m.ps;
       off = j - page * m.ps;
     }
+    // a page past the row's entries (a table narrower than the row; counted once per
+    // row where pt_n is set) is not read
+    if (page >= m.pt_n) return -1;
     const int32_t phys = m.pt_smem != nullptr ? m.pt_smem[page] : __ldg(m.pt_row + page);
     return phys * m.ps + off;
   } else if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) {
@@ -1456,6 +1461,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   OutMap m;
   m.pt_row = nullptr;
   m.pt_smem = nullptr;
+  m.pt_n = 0;
   m.ps = p.page_size;
   m.ps_shift = p.page_shift;
   m.rstart = 0;
@@ -1479,7 +1485,14 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     rowp = p.scores + static_cast<int64_t>(row) * p.row_stride;
     L = static_cast<int32_t>(min(static_cast<int64_t>(max(seq, 0)), p.row_stride));
   }
-  if constexpr (form_of(F) == kPaged) m.pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+  if constexpr (form_of(F) == kPaged) {
+    m.pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+    // the row's pages; a table row narrower than that is read only up to its stride
+    const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
+    const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
+    m.pt_n = static_cast<int32_t>(min(np, p.pt_stride));
+    if (np > p.pt_stride && rank == 0 && tid == 0) guard_hit();
+  }
   const int32_t k = p.k;
   int32_t* out = p.out + static_cast<int64_t>(row) * k;
 
@@ -1505,10 +1518,8 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // of a cluster, and rows of more than kPtCap pages, read it from global memory
   int32_t pages = 0;
   if constexpr (form_of(F) == kPaged) {
-    const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
-    const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
-    if (rank == 0 && np <= kPtCap) {
-      pages = static_cast<int32_t>(np);
+    if (rank == 0 && m.pt_n <= kPtCap) {
+      pages = m.pt_n;
       for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, m.pt_row + i);
     }
   }
@@ -1734,6 +1745,9 @@ __global__ void __launch_bounds__(kThreads) topk_sort_kernel(const Params p) {
   OutMap m;
   m.pt_row = form_of(F) == kPaged ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
   m.pt_smem = nullptr;
+  // every staged position lies on a page below the row's page count; entries past
+  // the table's row stride are not read (the selection kernel counted that row)
+  m.pt_n = static_cast<int32_t>(min(p.pt_stride, static_cast<int64_t>(INT32_MAX)));
   m.ps = p.page_size;
   m.ps_shift = p.page_shift;
   m.rstart = 0;

@@ -115,6 +115,15 @@ def test_grouped_layout_and_host_checks(lib):
             seq_lens=one, out=one, flags=pkg.TOPK_FLAG_SORTED)
     arr1 = (P * 1)(big)
     assert lib.topk_transform_grouped_static(ctypes.addressof(arr1), 1, None) == 3
+    # every problem is checked before the array's limit: a problem's own status wins
+    bad_k = P(form=0, batch=big.batch, k=2049, row_stride=8, scores=one, seq_lens=one,
+              out=one, flags=pkg.TOPK_FLAG_SORTED)
+    bad_form = P(form=5, batch=big.batch, k=2048, flags=pkg.TOPK_FLAG_SORTED)
+    for probs, status in (((bad_k,), 2), ((bad_form,), 1), ((big, bad_k), 2), ((big, bad_form), 1),
+                          ((bad_k, big), 2)):
+        arr2 = (P * len(probs))(*probs)
+        assert lib.topk_transform_grouped_static(ctypes.addressof(arr2), len(probs), None) == status
+        assert lib.topk_transform_grouped(ctypes.addressof(arr2), len(probs), None, 0, None) == status
     assert lib.topk_transform_grouped_static(None, 1, None) == 1
     assert lib.topk_transform_grouped_static(None, 0, None) == 0
 

@@ -134,6 +134,43 @@ def test_config5_long_rows(pkg, batch):
     assert_parity(w, run_gpu(pkg, w), check_rows=2)
 
 
+# ------------------------------------------------------------ a page table narrower than a row
+
+@pytest.mark.parametrize("split,fast", [(None, 1), (None, 0), (4, 1), (4, 0)])
+def test_paged_table_narrower_than_row(pkg, split, fast):
+    """Rows that need more pages than the table's row stride holds: the kernel reads
+    only the row's own entries, writes -1 for each selected position whose page is
+    missing, and counts each such row once in the guard counter (called through the C
+    ABI directly: the binding refuses such a table)."""
+    import ctypes
+    lib = pkg.load_library()
+    g = workloads.rng(4242)
+    B, S, ps, npt, k = 4, 8192, 64, 100, 1024
+    scores = workloads.random_rows(g, B, S, "normal")
+    seq = np.array([8192, 6400, 6000, 8000], np.int32)   # rows 0 and 3 need 128 and 125 pages
+    table = np.stack([g.permutation(4 * npt)[:npt] for _ in range(B)]).astype(np.int32)
+    raw = oracle.run(workloads.Workload("narrow_table_raw", "raw", k, scores, seq, None, ps))
+    page = np.where(raw >= 0, raw // ps, 0)
+    exp = np.where((raw >= 0) & (page < npt),
+                   np.take_along_axis(table, np.minimum(page, npt - 1), 1) * ps + raw % ps, -1)
+    dev = torch.device("cuda:0")
+    d_scores = torch.from_numpy(scores).to(dev)
+    d_seq = torch.from_numpy(seq).to(dev)
+    d_pt = torch.from_numpy(table).to(dev)
+    d_out = torch.full((B, k), -7, dtype=torch.int32, device=dev)
+    with settings(pkg, split=split, fast=fast):
+        st = lib.topk_transform_paged(ctypes.c_void_p(d_scores.data_ptr()), S,
+                                      ctypes.c_void_p(d_seq.data_ptr()),
+                                      ctypes.c_void_p(d_pt.data_ptr()), npt, ps, B, k,
+                                      ctypes.c_void_p(d_out.data_ptr()), None, 0, None)
+        torch.cuda.synchronize()
+    assert st == 0
+    got = d_out.cpu().numpy()
+    assert same_sets(got, exp).all()
+    assert pkg.topk_guard_hits() == 2  # one per row that needs more pages than the stride
+    pkg.topk_reset_guard_hits()
+
+
 # ------------------------------------------------------------ every execution path
 
 def _mixed(seed, dist, batch=6, stride=20000, k=1024, dup=True, form="paged"):
