@@ -53,13 +53,15 @@ REFERENCE_BUDGET_S = 120.0  # the reference arm's timed steps fit about this man
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=256)
     ap.add_argument("--form", choices=["paged", "raw"], default="paged")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=11,
+                    help="timed windows of exactly --steps calls; the median is reported")
     return ap.parse_args()
 
 
@@ -229,44 +231,63 @@ def call(pkg, w, d, stream):
         pkg.topk_transform_raw(d["scores"], d["seq"], w.k, out=d["out"], stream=stream)
 
 
-def time_steps(pkg, w, steps, warmup, dev, torch, l2_bytes, dist=None, clocks=None):
-    """Time exactly `steps` calls (CUDA graph replay over rotating input sets).
-    Returns (seconds, launches)."""
+def time_steps(pkg, w, steps, warmup, dev, torch, l2_bytes, dist=None, repeats=1):
+    """Time exactly `steps` calls, `repeats` times over. The calls cycle through R input
+    sets that together exceed L2_FACTOR x L2 (l2_bytes = 0: two sets, L2-hot); they are
+    replayed from two CUDA graphs, one over all R sets and one over the first
+    steps % R, so each timed window is exactly `steps` graph-launched calls. Each window
+    is bracketed by a device synchronise (and, under torchrun, a barrier) on both sides,
+    with CUDA events on the launching stream. Returns (seconds of each window, the
+    slowest rank's under torchrun; wall-clock span of the windows; R)."""
     set_bytes = w.scores.nbytes + w.seq_lens.nbytes + (w.page_table.nbytes if w.form == "paged" else 0)
     n_sets = max(2, min(4096, math.ceil(L2_FACTOR * l2_bytes / set_bytes)))
     sets = device_sets(w, n_sets, dev, torch)
     stream = torch.cuda.Stream(dev)
+    full, rest = divmod(steps, n_sets)
+    graphs = []
     with torch.cuda.stream(stream):
-        for i in range(max(warmup, 1)):
+        for i in range(max(warmup, 1)):  # untimed warm-up steps
             call(pkg, w, sets[i % n_sets], stream)
         stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for d in sets:
-                call(pkg, w, d, stream)
-        graph.replay()  # one untimed replay
+        for n, reps in ((n_sets, full), (rest, 1)):
+            if n == 0 or reps == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for d in sets[:n]:
+                    call(pkg, w, d, stream)
+            g.replay()  # one untimed replay
+            graphs.append((g, reps))
         stream.synchronize()
-    full, rest = divmod(steps, n_sets)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+    windows = []
     t0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(full):
-            graph.replay()
-        for i in range(rest):
-            call(pkg, w, sets[i], stream)
-        end.record(stream)
-    torch.cuda.synchronize(dev)
+    for _ in range(repeats):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for g, reps in graphs:
+                for _ in range(reps):
+                    g.replay()
+            end.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        secs = start.elapsed_time(end) / 1e3
+        windows.append(max_over_ranks(secs, dist, dev) if dist is not None else secs)
     t1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    secs = start.elapsed_time(end) / 1e3
-    del graph, sets
+    del graphs, sets
     torch.cuda.empty_cache()
-    return secs, steps, (t0, t1), n_sets
+    return windows, (t0, t1), n_sets
+
+
+def window_stats(windows, steps):
+    """Median, min and max microseconds per call over the timed windows."""
+    us = sorted(x / steps * 1e6 for x in windows)
+    return {"windows": len(us), "us_per_call_median": statistics.median(us),
+            "us_per_call_min": us[0], "us_per_call_max": us[-1]}
 
 
 def time_grouped(pkg, ws, steps, dev, torch, l2_bytes):
@@ -358,30 +379,34 @@ def time_e2e(pkg, w, steps, dev, torch):
     return secs, h2d, d2h
 
 
-def single_call_latency(pkg, dev, torch, calls: int = 200):
-    """One paged call at B=1 (c4_len=32768, k=1024) at a time, the stream idle
-    before each: the median device time between events around the call, and the
-    median host wall time from the call to its completion (launch included)."""
-    w = workload_for(1, "paged")
-    sets = device_sets(w, 2, dev, torch)
+def isolated_latency(pkg, w, dev, torch, l2_bytes, calls: int = 200):
+    """Device time of one call issued by itself: a spin kernel (torch.cuda._sleep) keeps
+    the stream busy while the host enqueues an event, the call and an event, so the
+    events bracket only the device's start of the call after the spin and the call
+    itself, not the binding's host work. Inputs rotate as in time_steps. Returns the
+    median and 10th/90th percentiles in microseconds."""
+    set_bytes = w.scores.nbytes + w.seq_lens.nbytes + (w.page_table.nbytes if w.form == "paged" else 0)
+    n_sets = max(2, min(64, math.ceil(L2_FACTOR * l2_bytes / set_bytes)))
+    sets = device_sets(w, n_sets, dev, torch)
     stream = torch.cuda.Stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dev_us, wall_us = [], []
+    us = []
     with torch.cuda.stream(stream):
         for i in range(calls + 10):
-            stream.synchronize()
-            t0 = time.perf_counter()
+            torch.cuda._sleep(100000)  # about 50 us of device time
             e0.record(stream)
-            call(pkg, w, sets[i % 2], stream)
+            call(pkg, w, sets[i % n_sets], stream)
             e1.record(stream)
-            stream.synchronize()
-            t1 = time.perf_counter()
+            e1.synchronize()
             if i >= 10:  # warm-up calls first
-                dev_us.append(e0.elapsed_time(e1) * 1e3)
-                wall_us.append((t1 - t0) * 1e6)
-    return {"batch": 1, "form": "paged", "workload": "B=1 single call (stream idle before it)",
-            "device_us_median": statistics.median(dev_us), "wall_us_median": statistics.median(wall_us),
-            "calls": calls}
+                us.append(e0.elapsed_time(e1) * 1e3)
+    del sets
+    torch.cuda.empty_cache()
+    us.sort()
+    return {"batch": w.batch, "form": w.form,
+            "workload": f"isolated call, B={w.batch} (stream idle before it)",
+            "us_median": statistics.median(us), "us_p10": us[len(us) // 10],
+            "us_p90": us[(9 * len(us)) // 10], "calls": calls, "input_sets": n_sets}
 
 
 def cpu_baseline(w, seconds: float = 1.5):
@@ -447,11 +472,11 @@ def run_ours(args):
 
     w = rank_workload(args.batch, args.form, rank)
     with ClockSampler(local) as clk:
-        secs, launches, (t0, t1), n_sets = time_steps(pkg, w, args.steps, args.warmup, dev, torch,
-                                                      l2, dist)
+        windows, (t0, t1), n_sets = time_steps(pkg, w, args.steps, args.warmup, dev, torch, l2,
+                                               dist, repeats=args.repeats)
         clocks = clk.summary(t0, t1)
-    if dist is not None:
-        secs = max_over_ranks(secs, dist, dev)
+    secs = statistics.median(windows)  # each window: exactly K steps, slowest rank's time
+    launches = args.steps
     per_call = secs / args.steps
     rows_per_s = world * w.batch * args.steps / secs
     gelem = world * w.scored_elements * args.steps / secs / 1e9
@@ -496,50 +521,49 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": e_secs / e2e_steps * 1e3},
         "clocks": clocks,
+        "repeats": window_stats(windows, args.steps),
         "gpu_launches": launches,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w)
     if rank == 0 and world == 1 and not args.no_sweep:
         sweep = []
+
+        def line(ws, steps, label=None, l2_bytes=l2, alg_bytes=None, repeats=5):
+            """One sweep entry: `repeats` windows of exactly `steps` calls, median and spread."""
+            win, _, ns = time_steps(pkg, ws, steps, 5, dev, torch, l2_bytes, repeats=repeats)
+            st = window_stats(win, steps)
+            pc = st["us_per_call_median"] / 1e6
+            ab = alg_bytes if alg_bytes is not None else workload_bytes(ws)
+            entry = {"batch": ws.batch, "form": ws.form}
+            if label is not None:
+                entry["workload"] = label
+            entry.update({"us_per_call": pc * 1e6, "us_per_call_min": st["us_per_call_min"],
+                          "us_per_call_max": st["us_per_call_max"], "windows": st["windows"],
+                          "rows_per_s": ws.batch / pc,
+                          "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
+                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+            return entry
+
         for (b, form) in ((1, "paged"), (8, "paged"), (64, "paged"), (128, "paged"),
                           (256, "paged"), (256, "raw"), (64, "raw")):
             if (b, form) == (w.batch, w.form):
                 continue
             ws = workload_for(b, form)
-            steps = 20000 if b >= 64 else 40000
-            s, _, _, ns = time_steps(pkg, ws, steps, 20, dev, torch, l2)
-            pc = s / steps
-            ab = algorithmic_bytes(b, C4_LEN, ws.k, form)
-            sweep.append({"batch": b, "form": form, "us_per_call": pc * 1e6,
-                          "rows_per_s": b / pc, "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
-                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+            sweep.append(line(ws, 4000 if b >= 64 else 8000,
+                              alg_bytes=algorithmic_bytes(b, C4_LEN, ws.k, form)))
         # the other configurations of the workload table, each timed the same way
         others = [("C1", workloads.config1()), ("C2 c4_len=8192", workloads.config2(8192)),
                   ("C2 c4_len=32768", workloads.config2(32768))]
         others += [(f"C4 {dist}", workloads.config4(dist)) for dist in ("banded", "narrow", "subnormal")]
         others += [(f"C5 B={b}", workloads.config5(b)) for b in (1, 2, 4)]
         for label, ws in others:
-            steps = 8192  # whole graph replays even for the smallest sets (4096 of them)
-            s, _, _, ns = time_steps(pkg, ws, steps, 5, dev, torch, l2)
-            pc = s / steps
-            ab = workload_bytes(ws)
-            sweep.append({"batch": ws.batch, "form": ws.form, "workload": f"{label}: {ws.name}",
-                          "us_per_call": pc * 1e6, "rows_per_s": ws.batch / pc,
-                          "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
-                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+            sweep.append(line(ws, 2000, label=f"{label}: {ws.name}"))
         # prefill-shaped window rows: 4096 queries over a 32768-key context, causal and
         # with a sliding window of 8192 keys
         for window in (None, 8192):
             ws = workloads.prefill_windows(4096, C4_LEN, window=window)
-            steps = 1000
-            s, _, _, ns = time_steps(pkg, ws, steps, 5, dev, torch, l2)
-            pc = s / steps
-            ab = workload_bytes(ws)
-            sweep.append({"batch": ws.batch, "form": "window", "workload": ws.name,
-                          "us_per_call": pc * 1e6, "rows_per_s": ws.batch / pc,
-                          "scored_gelem_per_s": ws.scored_elements / pc / 1e9,
-                          "gbs": ab / pc / 1e9, "frac": ab / pc / 1e9 / peak, "input_sets": ns})
+            sweep.append(line(ws, 200, label=ws.name))
         # several independent problems per step: four C3 paged batches of 64 rows, as
         # one grouped call (one launch) and as four calls
         ws4 = [workloads.config3(64, seed=workloads.BASE_SEED + 2 + 1000 * i) for i in range(4)]
@@ -548,21 +572,20 @@ def run_ours(args):
         sweep.append({"batch": 256, "form": "grouped", "workload": "4 x paged B=64 c4_len=32768 k=1024",
                       "us_per_call": tg * 1e6, "us_per_call_separate": tsep * 1e6,
                       "gbs": ab / tg / 1e9, "frac": ab / tg / 1e9 / peak})
-        # the headline workload with its inputs hot in L2 (two input sets replayed), and
-        # the latency of one call at B=1 issued by itself; labelled extras, never the
-        # headline (a failure here leaves the line intact)
+        # labelled extras, never the headline (a failure here leaves the line intact): the
+        # headline workload with its inputs hot in L2 (two input sets replayed), and the
+        # device time of single calls issued with the stream otherwise idle
         try:
-            s, _, _, ns = time_steps(pkg, w, 20000, 20, dev, torch, 0)
-            pc = s / 20000
-            sweep.append({"batch": w.batch, "form": w.form, "workload": "headline, L2-hot",
-                          "l2": f"hot: {ns} input sets ({ns * w.scores.nbytes / 1e6:.0f} MB) replayed",
-                          "us_per_call": pc * 1e6, "gbs": alg / pc / 1e9, "frac": alg / pc / 1e9 / peak})
+            e = line(w, 4000, label="headline, L2-hot", l2_bytes=0, alg_bytes=alg)
+            e["l2"] = f"hot: {e['input_sets']} input sets replayed"
+            sweep.append(e)
         except Exception as exc:  # noqa: BLE001
             sweep.append({"workload": "headline, L2-hot", "error": repr(exc)})
-        try:
-            sweep.append(single_call_latency(pkg, dev, torch))
-        except Exception as exc:  # noqa: BLE001
-            sweep.append({"workload": "B=1 single call", "error": repr(exc)})
+        for b in (1, 64, 256):
+            try:
+                sweep.append(isolated_latency(pkg, workload_for(b, "paged"), dev, torch, l2))
+            except Exception as exc:  # noqa: BLE001
+                sweep.append({"workload": f"isolated call, B={b}", "error": repr(exc)})
         result["sweep"] = sweep
     if rank == 0:
         print(json.dumps(result), flush=True)

@@ -274,6 +274,15 @@ int topk_reset_guard_hits(void);
  * threshold comes from a sample of the row and is verified afterwards; 0 always
  * runs the exact histogram tier. The result is the same either way.
  *
+ * topk_set_staged_tier(mode): where rows owned by one CTA whose length is known
+ * to be at most 32768 elements (row_stride for raw and paged, the length hints for
+ * ragged and window) run on the staged tier, which copies the row into shared
+ * memory from kernel start: 1 (default) automatically (launches of 64 rows up to
+ * one row per SM, rows that may hold 16384 elements or more); 2 always, with the
+ * whole row staged (one CTA per SM); 3 always, with half a row staged (two CTAs per
+ * SM); 0 never (the streaming fast tier). Other values mean 1. The result is the
+ * same either way.
+ *
  * topk_set_cta_threads(t): which build of the kernels runs: 512-thread CTAs (two
  * per SM) or 256-thread CTAs (four per SM, at most 3072 tie-buffer entries); any
  * other value restores the built-in choice, which takes the 256-thread build for
@@ -286,6 +295,7 @@ int topk_set_row_split(int g);
 int topk_set_tie_capacity(int cap);
 int topk_set_fast_tier(int enable);
 int topk_set_cta_threads(int threads);
+int topk_set_staged_tier(int mode);
 
 #ifdef __cplusplus
 } /* extern "C" */

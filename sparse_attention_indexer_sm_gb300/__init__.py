@@ -29,6 +29,7 @@ __all__ = [
     "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "TOPK_FLAG_SORTED",
     "topk_set_cta_threads", "topk_guard_hits", "topk_reset_guard_hits",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
+    "topk_set_staged_tier",
 ]
 
 TOPK_MAX_K = 2048
@@ -98,6 +99,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_set_cta_threads.argtypes = [ctypes.c_int]
             lib.topk_set_fast_tier.restype = ctypes.c_int
             lib.topk_set_fast_tier.argtypes = [ctypes.c_int]
+            lib.topk_set_staged_tier.restype = ctypes.c_int
+            lib.topk_set_staged_tier.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -388,3 +391,10 @@ def topk_set_cta_threads(threads: int) -> int:
 def topk_set_fast_tier(enable: bool) -> int:
     """1: try the sampled-threshold one-pass filter first (default); 0: exact tier only."""
     return int(load_library().topk_set_fast_tier(1 if enable else 0))
+
+
+def topk_set_staged_tier(mode: int) -> int:
+    """Where single-CTA rows of at most 32768 elements run on the staged tier (the row
+    copied to shared memory from kernel start): 1 automatic (default), 2 always with
+    the whole row staged, 3 always with half a row staged, 0 never."""
+    return int(load_library().topk_set_staged_tier(int(mode)))

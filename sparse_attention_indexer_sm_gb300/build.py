@@ -1,6 +1,6 @@
 """Build the CUDA library in-tree: sparse_attention_indexer_sm_gb300/_build/libtopk_transform.so.
 
-Both translation units are compiled for sm_103a only, in parallel, then linked
+Every object is compiled for sm_103a only, all of them in parallel, then linked
 against the shared CUDA runtime (so that the process keeps a single runtime
 together with PyTorch). Run ``python -m sparse_attention_indexer_sm_gb300.build``.
 """
@@ -19,7 +19,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libtopk_transform.so")
 
-SOURCES = ("topk_select.cu", "topk_select_cta256.cu", "topk_api.cu")
+SOURCES = ("topk_select.cu", "topk_api.cu")
+# The kernel source is compiled once per (CTA size, form) and once per CTA size for
+# the dispatch by form: ten objects that build in parallel.
+KERNEL_OBJECTS = [(f"topk_select_{cta}_{form}", ["-DTOPK_CTA_THREADS=%d" % cta, "-DTOPK_FORM=%d" % form])
+                  for cta in (512, 256) for form in range(4)]
+KERNEL_OBJECTS += [(f"topk_select_{cta}", ["-DTOPK_CTA_THREADS=%d" % cta]) for cta in (512, 256)]
 HEADERS = (os.path.join(CSRC, "topk_select.cuh"), os.path.join(INCLUDE, "topk_transform.h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -48,9 +53,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     exe = nvcc()
     procs, objs = [], []
-    for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [exe, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    units = [(name, defs, "topk_select.cu") for name, defs in KERNEL_OBJECTS]
+    units.append(("topk_api", [], "topk_api.cu"))
+    for name, defs, src in units:
+        obj = os.path.join(BUILD_DIR, name + ".o")
+        cmd = [exe, *NVCC_FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,

@@ -23,6 +23,7 @@ std::atomic<int> g_row_split{kRowSplitUnset};
 std::atomic<int> g_tie_cap{topk_gb300::kTieCapMax};
 std::atomic<int> g_fast_tier{1};
 std::atomic<int> g_cta_threads{0};  // 0: automatic; 512 or 256: that build
+std::atomic<int> g_staged{1};       // staged tier: 0 off, 1 automatic, 2 whole row, 3 half
 
 // The scratch of topk_transform_grouped_static: part of the module, one per device.
 // Host code must not hand this name to a kernel: on the host it is only a stand-in
@@ -94,6 +95,21 @@ bool use_cta256(int64_t rows, int64_t row_len, int g, int32_t k_max, int sm_coun
   const int64_t sms = sm_count;
   return g == 1 && rows > 2 * sms && k_max <= 1024 &&
          ((row_len > 0 && row_len <= 8192) || rows >= 16 * sms);
+}
+
+// Single-CTA rows of a known length of at most 32768 elements may run on the staged
+// tier of the 512-thread build (the row copied to shared memory from kernel start).
+// Returns 1 for the whole row staged (one CTA per SM), 2 for half a row (two CTAs per
+// SM), 0 for the streaming tiers. Automatically, launches of 64 rows up to one per
+// SM whose rows may hold 16384 elements or more take the whole-row variant (measured:
+// faster there; fewer or shorter rows, and launches of more rows, are faster on the
+// streaming tier).
+int use_staged(int g, int64_t rows, int64_t row_len, int use_filter, int sm_count) {
+  const int mode = g_staged.load(std::memory_order_relaxed);
+  if (g != 1 || use_filter == 0 || mode == 0 || !topk_gb300::cta512::staged_fits(row_len)) return 0;
+  if (mode == 2) return 1;
+  if (mode == 3) return 2;
+  return rows >= 64 && rows <= sm_count && row_len >= 16384 ? 1 : 0;
 }
 
 int fail_cuda(cudaError_t e) {
@@ -192,13 +208,14 @@ int run_one(const topk_problem_t& q, cudaStream_t stream) {
   cudaError_t e;
   if (use_cta256(p.batch, hint, g, p.k, ds->sm_count)) {
     p.tie_cap = std::min(p.tie_cap, topk_gb300::kTieCap256);
-    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, p.batch > ds->sm_count,
+    e = topk_gb300::cta256::launch(static_cast<Form>(q.form), p, g, p.batch > ds->sm_count, 0,
                                    stream);
   } else {
     // more rows than SMs: SMs hold two CTAs and the candidates' L2 read-back
-    // contends, so the filter reads them back from L1 instead (measured)
+    // contends, so the filter reads them back from L1 instead (measured); rows that
+    // fit in shared memory take the staged tier
     e = topk_gb300::cta512::launch(static_cast<Form>(q.form), p, g, p.batch > ds->sm_count,
-                                   stream);
+                                   use_staged(g, p.batch, hint, p.use_filter, ds->sm_count), stream);
   }
   return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
 }
@@ -353,10 +370,12 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
       for (int i = 0; i < gp.n; ++i)
         gp.probs[i].tie_cap = std::min(gp.probs[i].tie_cap, topk_gb300::kTieCap256);
       e = topk_gb300::cta256::launch_group(static_cast<Form>(f), gp, g, opts,
-                                           rows > ds->sm_count, stream);
+                                           rows > ds->sm_count, 0, stream);
     } else {
       e = topk_gb300::cta512::launch_group(static_cast<Form>(f), gp, g, opts,
-                                           rows > ds->sm_count, stream);
+                                           rows > ds->sm_count,
+                                           use_staged(g, rows, hint, knobs.use_filter, ds->sm_count),
+                                           stream);
     }
     if (e != cudaSuccess) return fail_cuda(e);
   }
@@ -445,6 +464,10 @@ int topk_set_row_split(int g) {
 
 int topk_set_fast_tier(int enable) {
   return g_fast_tier.exchange(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+}
+
+int topk_set_staged_tier(int mode) {
+  return g_staged.exchange(mode >= 0 && mode <= 3 ? mode : 1, std::memory_order_relaxed);
 }
 
 int topk_set_cta_threads(int threads) {

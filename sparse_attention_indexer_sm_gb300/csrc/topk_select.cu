@@ -62,10 +62,12 @@
 
 #include "topk_select.cuh"
 
-// This file is compiled twice: with TOPK_CTA_THREADS = 512 (namespace cta512: two
-// CTAs per SM, every launch that fits one wave) and 256 (cta256: four CTAs per SM,
-// for launches of more rows than that, so that each SM overlaps four rows'
-// latency chains instead of two).
+// This file is compiled for two CTA sizes: TOPK_CTA_THREADS = 512 (namespace cta512:
+// two CTAs per SM, every launch that fits one wave) and 256 (cta256: four CTAs per
+// SM, for launches of more rows than that, so that each SM overlaps four rows'
+// latency chains instead of two). For each size it is compiled once per form
+// (TOPK_FORM = 0 .. 3: that form's kernels and launches) and once without
+// TOPK_FORM (the dispatch by form), so that the objects build in parallel.
 #ifndef TOPK_CTA_THREADS
 #define TOPK_CTA_THREADS 512
 #endif
@@ -137,8 +139,12 @@ struct Ctl {
   uint32_t cls_cnt;                   // (winners, ties) slots of the candidate classification
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
+  uint32_t sup[32];                   // super-bin sums of the histogram being searched
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
   uint32_t xt[kMaxCluster];           // per-CTA threshold-bin elements
+  // staged tier
+  uint32_t wmax[kWarps], wmin[kWarps], wcnt[kWarps];  // per-warp sample extremes and size
+  uint32_t lam_lo, lam_hi, refine;    // the second sample round's window, and whether it runs
 };
 
 struct Sel {
@@ -383,19 +389,38 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
   __syncthreads();
 }
 
-// One warp (all 32 lanes) finds, in the padded kFastBins-bin histogram h, the
-// threshold bin for need1 (-> ctl.sel_*) and, if `two`, for need2 (-> ctl.sel2_*):
-// the bin where the count from the top reaches need (1 <= need <= sum of h). Lane
-// l first sums bins [32 l, 32 l + 32) (reads of 32 distinct banks, padded layout);
-// a suffix scan over the lanes names the lane whose range holds each threshold,
-// and the warp then scans that lane's 32 bins, one per lane, for both needs at once. The results are visible
-// to the block after the caller's next barrier.
+// Every warp of the CTA (a barrier at the end): the sums of the 32 super-bins of S
+// consecutive bins of the padded histogram h (32 S bins) into ctl.sup. A warp that
+// then searches h reads one word per lane instead of S: a lone warp's dependent
+// shared loads cost several thousand cycles at S = 32 or 64 (measured).
+template <int S>
+__device__ __forceinline__ void super_sums(const uint32_t* h, Ctl& ctl) {
+  constexpr int kPer = 32 / kWarps;  // super-bins per warp
+  static_assert(kPer * kWarps == 32 && S % 32 == 0, "super-bins split evenly");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int sb = warp * kPer + j;
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < S / 32; ++i) a += h[hist_index(sb * S + i * 32 + lane)];
+    a = __reduce_add_sync(kFull, a);
+    if (lane == 0) ctl.sup[sb] = a;
+  }
+  __syncthreads();
+}
+
+// One warp (all 32 lanes) finds, in the padded kFastBins-bin histogram h whose
+// super-bin sums (32 bins each) are in ctl.sup, the threshold bin for need1
+// (-> ctl.sel_*) and, if `two`, for need2 (-> ctl.sel2_*): the bin where the count
+// from the top reaches need (1 <= need <= sum of h). A suffix scan over the lanes'
+// super-bins names the super-bin holding each threshold, and the warp then scans
+// its 32 bins, one per lane, for both needs at once. The results are visible to the
+// block after the caller's next barrier.
 __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, uint32_t need2,
                                            bool two, Ctl& ctl) {
   const int lane = threadIdx.x & 31;
-  uint32_t s = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) s += h[hist_index(lane * 32 + i)];
+  const uint32_t s = ctl.sup[lane];  // bins [32 lane, 32 lane + 32)
   uint32_t x = s;  // count in the bins of lanes >= lane
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -407,8 +432,9 @@ __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, ui
   const uint32_t n2 = two ? need2 : need1;
   const uint32_t hit1 = __ballot_sync(kFull, s != 0 && excl < need1 && need1 <= x);
   const uint32_t hit2 = __ballot_sync(kFull, s != 0 && excl < n2 && n2 <= x);
-  if (hit1 == 0u || hit2 == 0u) return;  // a need outside [1, sum]: nothing to find
-  const int o1 = __ffs(hit1) - 1, o2 = __ffs(hit2) - 1;
+  // (a need outside [1, sum] finds nothing: no lane writes below; no early exit, as a
+  // lone warp pays an instruction fetch at every taken branch)
+  const int o1 = max(__ffs(hit1) - 1, 0), o2 = max(__ffs(hit2) - 1, 0);
   const uint32_t above1 = __shfl_sync(kFull, excl, o1), above2 = __shfl_sync(kFull, excl, o2);
   const int b1 = o1 * 32 + lane, b2 = o2 * 32 + lane;
   const uint32_t c1 = h[hist_index(b1)], c2 = h[hist_index(b2)];
@@ -425,30 +451,31 @@ __device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, ui
   const uint32_t a1 = above1 + y1 - c1, a2 = above2 + y2 - c2;
   const uint32_t here1 = __ballot_sync(kFull, c1 != 0 && a1 < need1 && need1 <= a1 + c1);
   const uint32_t here2 = __ballot_sync(kFull, c2 != 0 && a2 < n2 && n2 <= a2 + c2);
-  if (here1 != 0u && lane == __ffs(here1) - 1) {
+  const bool w1 = hit1 != 0u && here1 != 0u && lane == __ffs(here1) - 1;
+  const bool w2 = two && hit2 != 0u && here2 != 0u && lane == __ffs(here2) - 1;
+  if (w1) {
     ctl.sel_t = static_cast<uint32_t>(b1);
     ctl.sel_above = a1;
     ctl.sel_count = c1;
   }
-  if (two && here2 != 0u && lane == __ffs(here2) - 1) {
+  if (w2) {
     ctl.sel2_t = static_cast<uint32_t>(b2);
     ctl.sel2_above = a2;
     ctl.sel2_count = c2;
   }
 }
 
-// One warp (all 32 lanes) finds, in the padded kCandBins-bin candidate histogram h,
-// the bin where the count from the top reaches need (1 <= need <= sum of h) and
-// writes it to ctl.sel_* (visible to the block after the caller's next barrier):
-// lane l sums bins [P l, P l + P) (P = kCandBins / 32); a suffix scan over the lanes
-// names the owner of the threshold; then each lane takes P / 32 of the owner's bins.
+// One warp (all 32 lanes) finds, in the padded kCandBins-bin candidate histogram h
+// whose super-bin sums (P = kCandBins / 32 bins each) are in ctl.sup, the bin where
+// the count from the top reaches need (1 <= need <= sum of h) and writes it to
+// ctl.sel_* (visible to the block after the caller's next barrier): a suffix scan
+// over the lanes' super-bins names the one holding the threshold; then each lane
+// takes P / 32 of its bins.
 __device__ __forceinline__ void warp_find_cand(const uint32_t* h, uint32_t need, Ctl& ctl) {
-  constexpr int P = kCandBins / 32;  // bins per lane in the first step
+  constexpr int P = kCandBins / 32;  // bins of a super-bin
   constexpr int P2 = P / 32;         // bins per lane in the second step
   const int lane = threadIdx.x & 31;
-  uint32_t s = 0;
-#pragma unroll
-  for (int i = 0; i < P; ++i) s += h[hist_index(lane * P + i)];
+  const uint32_t s = ctl.sup[lane];  // bins [P lane, P lane + P)
   uint32_t x = s;  // count in the bins of lanes >= lane
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -456,8 +483,9 @@ __device__ __forceinline__ void warp_find_cand(const uint32_t* h, uint32_t need,
     if (lane + off < 32) x += y;
   }
   const uint32_t hit = __ballot_sync(kFull, s != 0 && x - s < need && need <= x);
-  if (hit == 0u) return;  // need outside [1, sum]: nothing to find
-  const int o = __ffs(hit) - 1;
+  // (need outside [1, sum] finds nothing: no lane writes below; straight-line code,
+  // as a lone warp pays an instruction fetch at every taken branch)
+  const int o = max(__ffs(hit) - 1, 0);
   const uint32_t above = __shfl_sync(kFull, x - s, o);
   const int b0 = o * P + lane * P2;  // this lane's bins [b0, b0 + P2) of the owner's range
   uint32_t c[P2];
@@ -473,19 +501,15 @@ __device__ __forceinline__ void warp_find_cand(const uint32_t* h, uint32_t need,
     const uint32_t z = __shfl_down_sync(kFull, y, off);
     if (lane + off < 32) y += z;
   }
-  uint32_t acc = above + y - s2;  // count above this lane's bins
+  const uint32_t acc = above + y - s2;  // count above this lane's bins
   const uint32_t here = __ballot_sync(kFull, s2 != 0 && acc < need && need <= acc + s2);
-  if (here != 0u && lane == __ffs(here) - 1) {
-#pragma unroll
-    for (int i = P2 - 1; i >= 0; --i) {
-      if (acc + c[i] >= need) {
-        ctl.sel_t = static_cast<uint32_t>(b0 + i);
-        ctl.sel_above = acc;
-        ctl.sel_count = c[i];
-        break;
-      }
-      acc += c[i];
-    }
+  // the owning lane's bin, from the top: the first whose count reaches need
+  static_assert(P2 == 2, "two bins per lane");
+  const bool upper = acc + c[1] >= need;
+  if (hit != 0u && here != 0u && lane == __ffs(here) - 1) {
+    ctl.sel_t = static_cast<uint32_t>(b0 + (upper ? 1 : 0));
+    ctl.sel_above = upper ? acc : acc + c[1];
+    ctl.sel_count = upper ? c[1] : c[0];
   }
 }
 
@@ -645,6 +669,12 @@ constexpr int kOpts = 4;
 // from L1 at once (instead of from L2 in a pass after the filter)
 constexpr int kSingle = 8;
 constexpr int kKeysInFilter = 16;
+// ... and kStaged for single-CTA rows on the staged tier (the whole row copied to
+// shared memory at kernel start; 512-thread build only)
+constexpr int kStaged = 32;
+// ... and kHalfStage with kStaged for the staged tier with half a row of staging
+// (two CTAs per SM)
+constexpr int kHalfStage = 64;
 __host__ __device__ constexpr int form_of(int F) { return F & 3; }
 __host__ __device__ constexpr bool opts_of(int F) { return (F & kOpts) != 0; }
 
@@ -789,6 +819,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   // the sample has arrived: now the bulk of the slice, issued by the last warp while
   // the first one looks for the thresholds
   if (!prefetched) prefetch_slice(s, kThreads - 32);
+  if (rank == 0) super_sums<32>((G > 1 ? mhist : hist) + kH1, ctl);
   // sample ranks a few standard deviations either side of the expected sample rank
   // of the row's k-th key
   uint32_t rs = 0, rs_lo = 0;
@@ -853,6 +884,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist + kH2, mhist + kH2, kFastWords);
+  if (rank == 0) super_sums<32>((G > 1 ? mhist : hist) + kH2, ctl);
   if (finder) {
     if (rs != 0)
       warp_find2((G > 1 ? mhist : hist) + kH2, rs - win_above, rs_lo - win_above, true, ctl);
@@ -1185,53 +1217,46 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
                                                   int32_t L, int32_t* out, const OutMap& m,
                                                   Ctl& ctl) {
   const int tid = threadIdx.x;
+  super_sums<kCandBins / 32>(chist, ctl);
   if (tid < 32) warp_find_cand(chist, k, ctl);
   __syncthreads();
   const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
-  if (ct > static_cast<uint32_t>(kListCap)) {
+  if (__builtin_expect(ct > static_cast<uint32_t>(kListCap), 0)) {
     select_in_buffer<F>(buf, n, k, 0ull, 64, L, out, static_cast<int32_t>(k), 0u, m, h, ctl);
     return;
   }
-  // candidates above the threshold bin are winners; the bin's go to the list. Each
-  // thread takes entries tid, tid + kThreads, ...; one reservation per warp of
-  // (winners, ties), packed in one word of ctl.cls_cnt, gives every slot.
-  constexpr int kPer = kTieCapMax / kThreads;
-  uint32_t cls = 0;  // bit 2r: winner, bit 2r+1: tie, for entry tid + r * kThreads
-  uint32_t nw = 0, nt = 0;
-#pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
-    if (i < n) {
-      const uint32_t b = min((buf[i].x - lambda) >> shift, static_cast<uint32_t>(kCandBins - 1));
-      if (b > t) {
-        cls |= 1u << (2 * r);
-        ++nw;
-      } else if (b == t) {
-        cls |= 2u << (2 * r);
-        ++nt;
-      }
-    }
-  }
-  const uint32_t off = warp_reserve(&ctl.cls_cnt, 0u, false, nw | (nt << 16));
-  uint32_t ws = off & 0xFFFFu, ts = off >> 16;
-#pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    const uint32_t c = (cls >> (2 * r)) & 3u;
-    const uint32_t i = static_cast<uint32_t>(tid) + r * kThreads;
-    if (c == 1u) {
-      if (ws < above) {
-        const uint2 e = buf[i];
+  // candidates above the threshold bin are winners; the bin's go to the list. The
+  // buffer is taken in warp-uniform rounds of kThreads entries (entry tid of each
+  // round); per round, each warp reserves its winners' and ties' slots at once (one
+  // atomic on the packed pair in ctl.cls_cnt) and each lane writes at its rank among
+  // the warp's, with no branch a lone lane would take.
+  const int lane = tid & 31;
+  for (uint32_t base = 0; base < n; base += kThreads) {
+    const uint32_t i = base + static_cast<uint32_t>(tid);
+    const bool live = i < n;
+    const uint2 e = live ? buf[i] : make_uint2(0u, 0u);
+    const uint32_t b = min((e.x - lambda) >> shift, static_cast<uint32_t>(kCandBins - 1));
+    const bool win = live && b > t, tie = live && b == t;
+    const uint32_t wm = __ballot_sync(kFull, win), tm = __ballot_sync(kFull, tie);
+    uint32_t off = 0;
+    if (lane == 0 && (wm | tm) != 0u)
+      off = atomicAdd(&ctl.cls_cnt, static_cast<uint32_t>(__popc(wm)) |
+                                        (static_cast<uint32_t>(__popc(tm)) << 16));
+    off = __shfl_sync(kFull, off, 0);
+    const uint32_t lt = lanemask_lt();
+    const uint32_t ws = (off & 0xFFFFu) + static_cast<uint32_t>(__popc(wm & lt));
+    const uint32_t ts = (off >> 16) + static_cast<uint32_t>(__popc(tm & lt));
+    if (win) {
+      if (ws < above)
         emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y), e.x);
-      } else {
-        guard_hit();
-      }
-      ++ws;
-    } else if (c == 2u) {
-      if (ts < ct)
-        list[ts] = buf[i];
       else
         guard_hit();
-      ++ts;
+    }
+    if (tie) {
+      if (ts < ct)
+        list[ts] = e;
+      else
+        guard_hit();
     }
   }
   __syncthreads();
@@ -1403,6 +1428,657 @@ __device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t
 
 // ------------------------------------------------------------------ the kernel
 
+// E1-E4: the exact tier over this CTA's slice s of a row of length L (CTA `rank` of
+// a cluster of G). hist and, in CTA 0, mhist are zero on entry; buf holds `cap`
+// (key, position) entries. Paged rows whose table was copied to shared memory
+// (pages > 0 entries at pt_smem) wait for that copy here if nothing waited before.
+template <int F>
+__device__ __forceinline__ void exact_tier(const Slice& s, int32_t L, int32_t k, int32_t* out,
+                                           OutMap m, int32_t pages, int32_t* pt_smem, int G,
+                                           int rank, uint32_t* hist, uint32_t* mhist, uint2* buf,
+                                           uint32_t cap, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  if constexpr (form_of(F) == kPaged) {
+    if (pages > 0 && m.pt_smem == nullptr) {  // the fast tier did not run
+      cp_async_wait_all();
+      __syncthreads();
+      m.pt_smem = pt_smem;
+    }
+  }
+  uint32_t need = static_cast<uint32_t>(k);  // winners still to find at or below the bin
+  uint32_t prefix = 0;                       // known high bits of the threshold key
+  int shift = 32;                            // prefix == threshold key >> shift
+  uint32_t cnt = static_cast<uint32_t>(L);   // elements whose key >> shift == prefix
+  uint32_t above_local = 0;                  // this CTA's elements above the bin
+  uint32_t tie_local = 0;                    // this CTA's elements in the bin
+  for (;;) {
+    const int w = min(kRowRoundBits, shift);
+    const int nshift = shift - w;
+    const uint32_t mask = (1u << w) - 1u;
+    if (shift != 32) {
+      for (int i = tid; i < hist_index(static_cast<int>(mask) + 1); i += kThreads) hist[i] = 0;
+      __syncthreads();
+    }
+    visit_keys(s, [&](bool ok, uint32_t key, int32_t) {
+      if (ok && __funnelshift_rc(key, 0u, shift) == prefix)
+        atomicAdd(&hist[hist_index(static_cast<int>((key >> nshift) & mask))], 1u);
+    });
+    __syncthreads();
+    const Sel sel = threshold_of(hist, mhist, 1 << w, need, G, rank, ctl);
+    if (G == 1) {
+      above_local += sel.above;
+      tie_local = sel.count;
+    } else {
+      uint32_t part = 0;
+      for (int i = tid; i <= static_cast<int>(mask); i += kThreads)
+        part += static_cast<uint32_t>(i) > sel.t ? hist[hist_index(i)] : 0u;
+      tie_local = hist[hist_index(static_cast<int>(sel.t))];
+      above_local += block_sum(part, ctl);
+    }
+    need -= sel.above;
+    prefix = (prefix << w) | sel.t;
+    shift = nshift;
+    cnt = sel.count;
+    if (cnt <= cap || shift == 0) break;
+  }
+
+  const uint32_t k_above = static_cast<uint32_t>(k) - need;  // winners above the bin
+  uint32_t win_base = 0, tie_base = 0;
+  if (G > 1) {
+    if (tid < G) {
+      dsmem_st(map_rank(smem_addr(&ctl.xa[rank]), tid), above_local);
+      dsmem_st(map_rank(smem_addr(&ctl.xt[rank]), tid), tie_local);
+    }
+    cluster_sync();
+    for (int r = 0; r < rank; ++r) {
+      win_base += ctl.xa[r];
+      tie_base += ctl.xt[r];
+    }
+  }
+
+  if (cnt <= cap) {
+    const bool remote = G > 1 && rank != 0;
+    const uint32_t ties_remote = G > 1 ? map_rank(smem_addr(buf), 0) : 0u;
+    scatter_pass<F>(s, prefix, shift, out, k, win_base, tie_base, buf, ties_remote, remote, cap, m,
+                    ctl);
+    if (G > 1)
+      cluster_sync();  // CTA 0 now holds every tie
+    else
+      __syncthreads();
+    if (rank == 0)
+      select_in_buffer<F>(buf, cnt, need, prefix, 32 + shift, L, out, k, k_above, m, hist, ctl);
+  } else {
+    // tie_base is this CTA's first position among the elements equal to prefix
+    const uint32_t quota = tie_base >= need ? 0u : min(need - tie_base, tie_local);
+    const uint32_t eq_slot0 = k_above + min(tie_base, need);
+    emit_equal<F>(s, prefix, out, k, win_base, eq_slot0, quota, m, ctl);
+  }
+}
+
+// ------------------------------------------------------------------ staged tier
+//
+// A row owned by one CTA whose aligned body holds at most kStagedQuads quads is
+// copied whole into shared memory, starting at kernel start. One SM takes in data
+// at a limited rate (about 25 bytes per clock, measured with plain and bulk loads
+// alike), and filtering a row takes the SM about as long again in integer work; so
+// the row must start arriving at once, and each part must be filtered as soon as it
+// has landed:
+//   - every thread first loads one quad of the sample: 16 runs of 512 bytes (one
+//     per warp) spread evenly over the row, 2048 keys for 512 threads;
+//   - the row is cut into chunks of kChunkQuads quads, one per thread, in passes of
+//     kPassChunks chunks; each thread copies its own quad of each chunk to shared
+//     memory with a 16-byte cp.async, one commit group per chunk. The first pass is
+//     asked for before lambda is looked for, the second after (a thread that has
+//     asked for much stalls until the memory system accepts its copies, and would
+//     find lambda late). With the whole row staged (one CTA per SM) the second pass
+//     has slots of its own; with half of it (two CTAs per SM) each thread copies
+//     the second pass into its own first-pass slots once it has read them, and the
+//     second half of the row is asked into L2 at kernel start;
+//   - lambda is found from the sample while the chunks arrive;
+//   - each thread flags its quad of each chunk that may hold a candidate (its
+//     largest or smallest element against the threshold) once the chunk's group
+//     has landed, then reads the flagged quads, about one in five, again for their
+//     exact candidates; each thread reads back only what it copied itself, so no
+//     barrier is needed;
+//   - each warp reserves its candidates' slots once per pass and writes their keys
+//     and positions into the candidate buffer and histogram.
+// For the raw and paged forms the copies cover the whole row stride and go out
+// before the row's length has arrived; elements at or past it are ignored.
+// Lambda comes from one round over the sample: the distance d = M - x in value of
+// each sample element from the sample's largest one is binned by its fp32 exponent
+// and the five bits after it (32 bins per power of two), in a window of 32 powers
+// of two that ends at the sample's range. Distances in value, unlike in key space,
+// do not jump where the scores change sign. If the bin holding the rs-th sample key
+// holds more than kRefineCount sample keys (scores packed into a narrow band), a
+// second round splits the window between the two sample ranks into 1024 equal key
+// bins. Any lambda gives an exact result (the candidate count is verified); these
+// only make the fast path likely. The candidate histogram and the selection are
+// those of the fast tier (F2, F3). If the candidate count does not verify, the exact
+// tier runs over the row.
+#if TOPK_CTA_THREADS == 512
+constexpr bool kHasStaged = true;
+#else
+constexpr bool kHasStaged = false;
+#endif
+constexpr int kChunkQuads = kThreads;                          // one quad per thread
+constexpr int kPassChunks = 8;                                 // chunks of one pass
+constexpr int kStagedChunks = 2 * kPassChunks;                 // chunks of a row at most
+constexpr int32_t kStagedQuads = kStagedChunks * kChunkQuads;  // 8192 quads (32768 elements)
+constexpr int kPtStaged = 512;                                 // page-table entries staged
+constexpr uint32_t kRefineCount = 32;                          // sample keys in a bin: refine
+constexpr int kLogSub = 5;                                     // bins per power of two: 2^kLogSub
+constexpr int kDistShift = 23 - kLogSub;                       // fp32 bits below a log bin
+// Shared memory of the staged tier (words): staging | sample histogram (1024 bins)
+// | candidate histogram (2048 bins; also the second sample round's) | page table |
+// candidate buffer. The staging area holds the whole row (kStagedChunks chunks: one
+// CTA per SM) or half of it (kPassChunks chunks, two CTAs per SM: the second pass
+// reuses the first pass's slots). Once the candidates are in the buffer, it holds
+// the list of threshold-bin entries and the scratch histogram of the selection (or
+// the exact tier's histogram).
+template <bool kHalf>
+__host__ __device__ constexpr int stage_words() { return (kHalf ? kPassChunks : kStagedChunks) * kChunkQuads * 4; }
+template <bool kHalf>
+__host__ __device__ constexpr int staged_fixed_words() { return stage_words<kHalf>() + kFastWords + kCandWords + kPtStaged; }
+static_assert(kListWords + kHistWords <= stage_words<true>(), "list and scratch must fit the staging area");
+
+
+// 128-bit read-only load issued where it stands (volatile: the compiler may not move
+// it towards its use).
+__device__ __forceinline__ uint4 ld_now(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t quad_elem(const uint4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// One candidate: its key into the buffer at `slot` (if below cap) and into the
+// candidate histogram; the last bin is counted per lane (top).
+__device__ __forceinline__ void staged_put(uint32_t bits, int32_t j, uint32_t slot, uint32_t lambda,
+                                           uint32_t shift, uint2* buf, uint32_t cap,
+                                           uint32_t* chist, uint32_t& top) {
+  const uint32_t key = order_key(bits);
+  const uint32_t d = (key - lambda) >> shift;
+  if (d >= static_cast<uint32_t>(kCandBins - 1))
+    ++top;
+  else
+    atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+  if (slot < cap) buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
+}
+
+// Candidate mask of quad v, quad q of the body whose first element is at row
+// position j (bit c: element c is a candidate at a position below L).
+template <bool kPos>
+__device__ __forceinline__ uint32_t quad_cands(const uint4& v, int32_t q, int32_t nvec, int32_t j,
+                                               int32_t L, uint32_t thr) {
+  if (q >= nvec) return 0u;
+  const int32_t left = L - j;  // elements of the quad below L
+  const uint32_t lm = left >= 4 ? 0xFu : left <= 0 ? 0u : (1u << left) - 1u;
+  return lm & (static_cast<uint32_t>(is_candidate<kPos>(v.x, thr)) |
+               (static_cast<uint32_t>(is_candidate<kPos>(v.y, thr)) << 1) |
+               (static_cast<uint32_t>(is_candidate<kPos>(v.z, thr)) << 2) |
+               (static_cast<uint32_t>(is_candidate<kPos>(v.w, thr)) << 3));
+}
+
+// Asynchronous 16-byte copy global -> shared (both 16-byte aligned), L2 only.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
+// This thread's quads of chunks [c0, c0 + kPassChunks) of the body (vb, nvec quads)
+// into slots [slot0, slot0 + kPassChunks) of the staging area, one commit group per
+// chunk (empty for chunks past the body).
+__device__ __forceinline__ void copy_pass(uint4* stage, int slot0, int c0, const uint4* vb,
+                                          int32_t nvec) {
+#pragma unroll
+  for (int i = 0; i < kPassChunks; ++i) {
+    const int32_t q = (c0 + i) * kChunkQuads + static_cast<int32_t>(threadIdx.x);
+    if (q < nvec) cp_async16(stage + (slot0 + i) * kChunkQuads + threadIdx.x, vb + q);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// Waits until this thread's copy groups up to pass chunk i have landed, when kLater
+// groups were committed after the pass's last chunk (i and kLater compile-time).
+template <int kLater>
+__device__ __forceinline__ void wait_pass_chunk(int i) {
+  switch (i) {
+    case 0: cp_async_wait_group<kLater + kPassChunks - 1>(); break;
+    case 1: cp_async_wait_group<kLater + kPassChunks - 2>(); break;
+    case 2: cp_async_wait_group<kLater + kPassChunks - 3>(); break;
+    case 3: cp_async_wait_group<kLater + kPassChunks - 4>(); break;
+    case 4: cp_async_wait_group<kLater + kPassChunks - 5>(); break;
+    case 5: cp_async_wait_group<kLater + kPassChunks - 6>(); break;
+    case 6: cp_async_wait_group<kLater + kPassChunks - 7>(); break;
+    default: cp_async_wait_group<kLater>(); break;
+  }
+}
+static_assert(kPassChunks == 8, "wait_pass_chunk spells out eight chunks");
+
+// Whether quad v may hold a candidate: its largest element (signed compare, kPos) or
+// its smallest (unsigned) against the filter threshold. Positions past the body or
+// the row's length are not looked at here; the exact mask is taken afterwards.
+template <bool kPos>
+__device__ __forceinline__ bool quad_may(const uint4& v, uint32_t thr) {
+  if constexpr (kPos) {
+    const int32_t mx = max(max(static_cast<int32_t>(v.x), static_cast<int32_t>(v.y)),
+                           max(static_cast<int32_t>(v.z), static_cast<int32_t>(v.w)));
+    return mx >= static_cast<int32_t>(thr);
+  } else {
+    return min(min(v.x, v.y), min(v.z, v.w)) <= thr;
+  }
+}
+
+// F2 on one pass of staged chunks (every thread), in two levels: this thread's quad
+// of each chunk c0 + i (slot slot0 + i) is flagged if it may hold a candidate, once
+// the chunk's copy group has landed (kLater groups were committed after the pass);
+// then the flagged quads, about one in five, are read again for their exact
+// candidates (positions below L), which go with this thread's edge element (when
+// `edge`) to buf / chist at slots from one reservation per warp on ctl.cand_cnt.
+template <bool kPos, int kLater>
+__device__ __forceinline__ void filter_pass(const uint4* stage, int slot0, int c0, int32_t nvec,
+                                            int32_t head, int32_t L, bool edge, int32_t ej,
+                                            uint32_t ebits, uint32_t lambda, uint32_t shift,
+                                            uint2* buf, uint32_t cap, uint32_t* chist,
+                                            uint32_t& top, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
+  uint32_t fl = 0;  // bit i: this thread's quad of pass chunk i may hold a candidate
+#pragma unroll
+  for (int i = 0; i < kPassChunks; ++i) {
+    wait_pass_chunk<kLater>(i);
+    fl |= static_cast<uint32_t>(quad_may<kPos>(stage[(slot0 + i) * kChunkQuads + tid], thr)) << i;
+  }
+  // exact masks of the flagged quads: bits 4 i .. 4 i + 3 for pass chunk i
+  uint32_t m = 0;
+  while (fl != 0u) {
+    const int i = __ffs(fl) - 1;
+    fl &= fl - 1u;
+    const int32_t q = (c0 + i) * kChunkQuads + tid;
+    m |= quad_cands<kPos>(stage[(slot0 + i) * kChunkQuads + tid], q, nvec, head + 4 * q, L, thr)
+         << (4 * i);
+  }
+  const bool ec = edge && is_candidate<kPos>(ebits, thr);
+  uint32_t slot = warp_reserve(&ctl.cand_cnt, 0u, false,
+                               static_cast<uint32_t>(__popc(m)) + (ec ? 1u : 0u));
+  if (ec) staged_put(ebits, ej, slot++, lambda, shift, buf, cap, chist, top);
+  while (m != 0u) {
+    const int bit = __ffs(m) - 1;
+    m &= m - 1u;
+    const int i = bit >> 2, e = bit & 3;
+    const int32_t q = (c0 + i) * kChunkQuads + tid;
+    staged_put(quad_elem(stage[(slot0 + i) * kChunkQuads + tid], e), head + 4 * q + e, slot++, lambda,
+               shift, buf, cap, chist, top);
+  }
+}
+
+// The second sample round of staged_lambda (every thread; the same sample quad v at
+// row position j, `in` as there): 1024 equal key bins over [ctl.lam_lo, ctl.lam_hi]
+// (keys above it counted apart) in chist's region, which is cleared again
+// afterwards; ctl.lambda and ctl.lambda_shift are updated. Kept out of line, as it
+// runs only for scores packed into a narrow band.
+__device__ __noinline__ void staged_refine(uint4 v, int32_t j, bool in, int32_t L, uint32_t rs,
+                                           uint32_t rs_lo, uint32_t* chist, Ctl& ctl) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t wlo = ctl.lam_lo, whi = ctl.lam_hi;
+  const int f = max(0, (32 - __clz(static_cast<int>(whi - wlo))) - kFastBits);
+  uint32_t above = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (!(in && j + c < L)) continue;
+    const uint32_t key = order_key(quad_elem(v, c));
+    if (key > whi)
+      ++above;
+    else if (key >= wlo)
+      atomicAdd(&chist[hist_index(static_cast<int>((key - wlo) >> f))], 1u);
+  }
+  above = __reduce_add_sync(kFull, above);
+  __syncthreads();  // every thread has read ctl.refine and the window
+  if (lane == 0) ctl.wcnt[warp] = above;
+  __syncthreads();
+  uint32_t na = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) na += ctl.wcnt[w];
+  super_sums<32>(chist, ctl);
+  if (warp == 0 && rs > na) {  // else rs lies above the window (rounding): round 1 stands
+    const bool two = rs_lo > na;
+    warp_find2(chist, rs - na, two ? rs_lo - na : rs - na, two, ctl);
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t lam = wlo + (ctl.sel_t << f);
+      const uint64_t top =
+          static_cast<uint64_t>(wlo) + (static_cast<uint64_t>(ctl.sel2_t + 1u) << f) - 1u;
+      const uint32_t hi = two ? static_cast<uint32_t>(min(top, static_cast<uint64_t>(whi))) : whi;
+      const uint32_t gap = hi > lam ? hi - lam : 0u;
+      ctl.lambda = lam;
+      ctl.lambda_shift =
+          static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kCandWords; i += kThreads) chist[i] = 0;
+  __syncthreads();
+}
+
+// Lambda from the sample (every thread of the CTA; thread t holds sample quad v,
+// whose first element is at row position j, when `in`). shist is zero on entry;
+// chist is zero on entry and on return. Returns lambda; *shift gets the
+// candidate-histogram bin width exponent.
+__device__ __forceinline__ uint32_t staged_lambda(const uint4& v, int32_t j, bool in, int32_t L,
+                                                  uint32_t k, uint32_t* shist, uint32_t* chist,
+                                                  Ctl& ctl, uint32_t* shift) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t key[4];
+  bool ok[4];
+  uint32_t mx = 0, mn = 0xFFFFFFFFu, cnt = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    key[c] = order_key(quad_elem(v, c));
+    ok[c] = in && j + c < L;
+    if (ok[c]) {
+      mx = max(mx, key[c]);
+      mn = min(mn, key[c]);
+      ++cnt;
+    }
+  }
+  mx = __reduce_max_sync(kFull, mx);
+  mn = __reduce_min_sync(kFull, mn);
+  cnt = __reduce_add_sync(kFull, cnt);
+  if (lane == 0) {
+    ctl.wmax[warp] = mx;
+    ctl.wmin[warp] = mn;
+    ctl.wcnt[warp] = cnt;
+  }
+  __syncthreads();
+  // the CTA's values: lane l < kWarps reads warp l's, then a warp reduction
+  const bool own = lane < kWarps;
+  const uint32_t M = __reduce_max_sync(kFull, own ? ctl.wmax[lane] : 0u);
+  const uint32_t Mn = __reduce_min_sync(kFull, own ? ctl.wmin[lane] : 0xFFFFFFFFu);
+  const uint32_t ns = __reduce_add_sync(kFull, own ? ctl.wcnt[lane] : 0u);
+  // round 1: log bins of the distance in value from the largest sample element, in
+  // the 32 powers of two below the sample's range (index 1023 - bin, so that larger
+  // scores have higher indices); distances past the window share its end bins
+  const float Mv = __uint_as_float(key_bits(M));
+  const float range = Mv - __uint_as_float(key_bits(Mn));
+  const bool usable = ns != 0 && isfinite(range);
+  const int32_t base = static_cast<int32_t>(__float_as_uint(range) >> kDistShift) + 1 - (kFastBins - 1);
+  if (usable) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (!ok[c]) continue;
+      const float d = Mv - __uint_as_float(key_bits(key[c]));
+      // NaN and infinite distances (non-finite scores) fall into the last bin
+      const int32_t raw = isfinite(d) ? static_cast<int32_t>(__float_as_uint(d) >> kDistShift)
+                                      : INT32_MAX - kFastBins;
+      const int32_t bin = min(max(raw - base, 0), kFastBins - 1);
+      atomicAdd(&shist[hist_index(kFastBins - 1 - bin)], 1u);
+    }
+  }
+  __syncthreads();
+  // the sample ranks: four standard deviations below the expected sample rank of the
+  // row's k-th key (lambda's side) and three above (the candidate-histogram width)
+  uint32_t rs = 0, rs_lo = 0;
+  if (usable) {
+    const float mean =
+        fmaxf(__fdividef(static_cast<float>(k) * static_cast<float>(ns), static_cast<float>(L)), 1.0f);
+    const float sd = mean * rsqrtf(mean);
+    rs = min(static_cast<uint32_t>(ceilf(mean + 4.0f * sd)) + 2u, ns);
+    const float lo = floorf(mean - 3.0f * sd);
+    rs_lo = min(lo < 1.0f ? 1u : static_cast<uint32_t>(lo), rs);
+  }
+  super_sums<32>(shist, ctl);
+  if (warp == 0) {
+    if (usable) warp_find2(shist, rs, rs_lo, true, ctl);
+    __syncwarp();
+    if (lane == 0) {
+      uint32_t refine = 0;
+      if (usable) {
+        // the distances at a window bin's edges (bins 0 and kFastBins - 1 are open)
+        const int32_t bs = kFastBins - 1 - static_cast<int32_t>(ctl.sel_t);
+        const int32_t bl = kFastBins - 1 - static_cast<int32_t>(ctl.sel2_t);
+        const int32_t ehi = bs + base + 1, elo = bl + base;
+        const float dhi = bs >= kFastBins - 1 ? __uint_as_float(0x7F800000u)
+                          : ehi <= 0          ? 0.0f
+                                              : __uint_as_float((static_cast<uint32_t>(ehi) << kDistShift) - 1u);
+        const float dlo = bl <= 0 || elo <= 0 ? 0.0f
+                                              : __uint_as_float(static_cast<uint32_t>(elo) << kDistShift);
+        // keys of M - d, lambda rounded down and lambda_hi up by a few key units
+        const float xlo = Mv - dhi, xhi = Mv - dlo;
+        const uint32_t klo = isnan(xlo) ? 0u : order_key(__float_as_uint(xlo));
+        const uint32_t khi = isnan(xhi) ? M : order_key(__float_as_uint(xhi));
+        const uint32_t lam = klo > 2u ? klo - 2u : 0u;
+        const uint32_t lam_hi = min(khi + 2u < khi ? khi : khi + 2u, M);
+        ctl.lambda = lam;
+        ctl.lam_lo = lam;  // the second round's window: [lam, lam_hi]
+        ctl.lam_hi = lam_hi;
+        refine = ctl.sel_count > kRefineCount && lam_hi > lam ? 1u : 0u;
+        const uint32_t gap = lam_hi > lam ? lam_hi - lam : 0u;
+        ctl.lambda_shift =
+            static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
+      } else {
+        ctl.lambda = 0;
+        ctl.lambda_shift = 32 - kCandBits;
+      }
+      ctl.refine = refine;
+    }
+  }
+  __syncthreads();
+  if (__builtin_expect(ctl.refine != 0u, 0)) staged_refine(v, j, in, L, rs, rs_lo, chist, ctl);
+  *shift = ctl.lambda_shift;
+  return ctl.lambda;
+}
+
+// One row of problem p on the staged tier (one CTA, no cluster).
+template <int F>
+__device__ __forceinline__ void staged_row(const Params& p, int row, uint32_t* dyn, Ctl& ctl) {
+  constexpr bool kHalf = (F & kHalfStage) != 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint4* stage = reinterpret_cast<uint4*>(dyn);
+  uint32_t* shist = dyn + stage_words<kHalf>();   // sample histogram (kFastBins, padded)
+  uint32_t* chist = shist + kFastWords;            // candidate histogram (kCandBins, padded)
+  int32_t* pt_smem = reinterpret_cast<int32_t*>(chist + kCandWords);
+  uint2* buf = reinterpret_cast<uint2*>(pt_smem + kPtStaged);
+  const uint32_t cap = static_cast<uint32_t>(p.tie_cap);
+
+  allow_next_grid();
+  for (int i = tid; i < kFastWords + kCandWords; i += kThreads) shist[i] = 0;
+  if (tid == 0) {
+    ctl.win_cnt = 0;
+    ctl.tie_cnt = 0;
+    ctl.out_cnt = 0;
+    ctl.cand_cnt = 0;
+    ctl.cls_cnt = 0;
+  }
+  __syncthreads();  // cleared memory before any use
+  wait_prior_grids();
+
+  const int32_t seq = p.seq_lens[row];
+  int32_t start = 0;
+  if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) start = p.row_starts[row];
+
+  // the row's data and the length its layout covers: raw and paged rows lay out the
+  // whole stride at once; ragged and window rows wait for their start and length
+  const float* rowp;
+  int32_t span;
+  if constexpr (form_of(F) == kRagged) {
+    rowp = p.scores + start;
+    span = max(seq, 0);
+  } else if constexpr (form_of(F) == kWindow) {
+    const int64_t hi = min(static_cast<int64_t>(max(seq, 0)), p.row_stride);
+    const int64_t lo = min(static_cast<int64_t>(max(start, 0)), hi);
+    rowp = p.scores + static_cast<int64_t>(row) * p.row_stride + lo;
+    span = static_cast<int32_t>(hi - lo);
+  } else {
+    rowp = p.scores + static_cast<int64_t>(row) * p.row_stride;
+    span = static_cast<int32_t>(p.row_stride);
+  }
+  const Slice lay = make_slice(rowp, span, 0, 1);
+  const uint4* vb = lay.vec;  // the aligned body: nvec quads from row position head
+  const int32_t nvec = lay.nvec, head = lay.n_head;
+  const bool fits = nvec <= kStagedQuads;
+  // the sample first (run `warp` of 16 spread over the body), then the early chunks
+  const int32_t qs = static_cast<int32_t>((static_cast<int64_t>(nvec) * warp) / kWarps) + lane;
+  const bool sin = fits && qs < nvec;
+  const uint4 sv = sin ? ld_now(vb + qs) : make_uint4(0, 0, 0, 0);
+  if (fits) copy_pass(stage, 0, 0, vb, nvec);
+  if constexpr (kHalf) {  // the second half towards L2, from the last warp
+    const int32_t q1 = min(nvec, kPassChunks * kChunkQuads);
+    const uint32_t bytes = fits ? 16u * static_cast<uint32_t>(nvec - q1) : 0u;
+    const uint32_t piece = static_cast<uint32_t>(kPrefetchBytes);
+    const uint32_t off = static_cast<uint32_t>(tid - (kThreads - 32)) * piece;
+    if (tid >= kThreads - 32 && off < bytes)
+      prefetch_l2(reinterpret_cast<const char*>(vb + q1) + off, min(piece, bytes - off));
+  }
+  // paged: the page table of the span's pages (at most the table's row stride)
+  int32_t pages = 0;
+  if constexpr (form_of(F) == kPaged) {
+    const int64_t up = static_cast<int64_t>(span) + p.page_size - 1;
+    const int64_t np = min(p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size, p.pt_stride);
+    if (np <= kPtStaged) {
+      pages = static_cast<int32_t>(np);
+      const int32_t* pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+      for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, pt_row + i);
+    }
+  }
+
+  OutMap m;
+  m.pt_row = nullptr;
+  m.pt_smem = nullptr;
+  m.pt_n = 0;
+  m.ps = p.page_size;
+  m.ps_shift = p.page_shift;
+  m.rstart = 0;
+  m.values = opts_of(F) && p.values != nullptr ? p.values + static_cast<int64_t>(row) * p.k
+                                               : nullptr;
+  m.staged = opts_of(F) && p.staged != nullptr ? p.staged + static_cast<int64_t>(row) * p.k
+                                               : nullptr;
+  int32_t L;
+  if constexpr (form_of(F) == kRagged) {
+    m.rstart = start;
+    L = span;
+  } else if constexpr (form_of(F) == kWindow) {
+    m.rstart = static_cast<int32_t>(rowp - (p.scores + static_cast<int64_t>(row) * p.row_stride));
+    L = span;
+  } else {
+    L = static_cast<int32_t>(min(static_cast<int64_t>(max(seq, 0)), p.row_stride));
+  }
+  if constexpr (form_of(F) == kPaged) {
+    m.pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+    const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
+    const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
+    m.pt_n = static_cast<int32_t>(min(np, p.pt_stride));
+    if (np > p.pt_stride && tid == 0) guard_hit();
+  }
+  const int32_t k = p.k;
+  int32_t* out = p.out + static_cast<int64_t>(row) * k;
+
+  if (__builtin_expect(!fits, 0)) {  // a ragged or window row longer than its hint promised
+    cp_async_wait_all();
+    for (int i = tid; i < kHistWords; i += kThreads) dyn[i] = 0;
+    __syncthreads();
+    exact_tier<F>(make_slice(rowp, L, 0, 1), L, k, out, m, pages, pt_smem, 1, 0, dyn, nullptr, buf,
+                  cap, ctl);
+    return;
+  }
+
+  if (__builtin_expect(L <= k, 0)) {  // every position is selected; the rest of the row is -1
+    const bool keys = opts_of(F) && (m.values != nullptr || m.staged != nullptr);
+    for (int32_t i = tid; i < k; i += kThreads) {
+      if (i < L)
+        emit<F>(out, k, static_cast<uint32_t>(i), m, i, keys ? order_key(__float_as_uint(rowp[i])) : 0u);
+      else
+        emit_pad<F>(out, static_cast<uint32_t>(i), m);
+    }
+    cp_async_wait_all();  // nothing may still be copying into shared memory at exit
+    return;
+  }
+
+  // this thread's unaligned head or tail element, if any: positions [0, head) and
+  // [head + 4 nvec, L)
+  int32_t ej = 0;
+  bool edge = false;
+  {
+    const int32_t tail0 = head + 4 * nvec;
+    if (tid < head && tid < L) {
+      ej = tid;
+      edge = true;
+    } else if (tid >= 4 && tid - 4 < L - tail0) {
+      ej = tail0 + (tid - 4);
+      edge = true;
+    }
+  }
+  const uint32_t ebits = edge ? __float_as_uint(rowp[ej]) : 0u;
+
+  // ---- lambda from the sample (rows that fit the buffer: every element)
+  uint32_t lambda = 0, shift2 = 32 - kCandBits;
+  if (static_cast<uint32_t>(L) > cap)
+    lambda = staged_lambda(sv, head + 4 * qs, sin, L, static_cast<uint32_t>(k), shist, chist, ctl,
+                           &shift2);
+
+  // ---- the second pass's copies, and the filter of each chunk as it lands
+  uint32_t top = 0;
+  const bool pos = lambda >= 0x80000000u;
+  if constexpr (!kHalf) {  // the whole row in the staging area
+    copy_pass(stage, kPassChunks, kPassChunks, vb, nvec);
+    if (pos) {
+      filter_pass<true, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf,
+                                     cap, chist, top, ctl);
+      filter_pass<true, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2,
+                           buf, cap, chist, top, ctl);
+    } else {
+      filter_pass<false, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf,
+                                      cap, chist, top, ctl);
+      filter_pass<false, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda,
+                            shift2, buf, cap, chist, top, ctl);
+    }
+  } else {  // half the row: the second pass into this thread's first-pass slots
+    if (pos)
+      filter_pass<true, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf, cap, chist,
+                           top, ctl);
+    else
+      filter_pass<false, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf, cap,
+                            chist, top, ctl);
+    copy_pass(stage, 0, kPassChunks, vb, nvec);
+    if (pos)
+      filter_pass<true, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2, buf, cap,
+                           chist, top, ctl);
+    else
+      filter_pass<false, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2, buf,
+                            cap, chist, top, ctl);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
+  if (lane == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
+  cp_async_wait_all();  // the page table
+  if constexpr (form_of(F) == kPaged) {
+    if (pages > 0) m.pt_smem = pt_smem;  // visible to all threads after the barrier below
+  }
+  __syncthreads();
+  const uint32_t n_cand = ctl.cand_cnt;
+  uint2* list = reinterpret_cast<uint2*>(dyn);  // the staging area is free from here on
+  uint32_t* scratch = dyn + kListWords;
+  if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
+    select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list, scratch,
+                         L, out, m, ctl);
+    return;
+  }
+  // too few (lambda above the k-th key) or too many candidates: exact tier
+  for (int i = tid; i < kHistWords; i += kThreads) dyn[i] = 0;
+  __syncthreads();
+  exact_tier<F>(make_slice(rowp, L, 0, 1), L, k, out, m, pages, pt_smem, 1, 0, dyn, nullptr, buf,
+                cap, ctl);
+}
+
 // One row of problem p, this CTA's slice of it (CTA `rank` of a cluster of G).
 template <int F>
 __device__ __forceinline__ void row_body(const Params& p, int row, int G, int rank, uint32_t* dyn,
@@ -1573,7 +2249,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
       n_cand = ctl.n_cand;
       chist = mhist + kHC;
     }
-    if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap) {
+    if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
       if (rank == 0)
         select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
                              hist, L, out, m, ctl);
@@ -1591,81 +2267,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   }
 
   // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
-  if constexpr (form_of(F) == kPaged) {
-    if (pages > 0 && m.pt_smem == nullptr) {  // the fast tier did not run
-      cp_async_wait_all();
-      __syncthreads();
-      m.pt_smem = pt_smem;
-    }
-  }
-  uint32_t need = static_cast<uint32_t>(k);  // winners still to find at or below the bin
-  uint32_t prefix = 0;                       // known high bits of the threshold key
-  int shift = 32;                            // prefix == threshold key >> shift
-  uint32_t cnt = static_cast<uint32_t>(L);   // elements whose key >> shift == prefix
-  uint32_t above_local = 0;                  // this CTA's elements above the bin
-  uint32_t tie_local = 0;                    // this CTA's elements in the bin
-  for (;;) {
-    const int w = min(kRowRoundBits, shift);
-    const int nshift = shift - w;
-    const uint32_t mask = (1u << w) - 1u;
-    if (shift != 32) {
-      for (int i = tid; i < hist_index(static_cast<int>(mask) + 1); i += kThreads) hist[i] = 0;
-      __syncthreads();
-    }
-    visit_keys(s, [&](bool ok, uint32_t key, int32_t) {
-      if (ok && __funnelshift_rc(key, 0u, shift) == prefix)
-        atomicAdd(&hist[hist_index(static_cast<int>((key >> nshift) & mask))], 1u);
-    });
-    __syncthreads();
-    const Sel sel = threshold_of(hist, mhist, 1 << w, need, G, rank, ctl);
-    if (G == 1) {
-      above_local += sel.above;
-      tie_local = sel.count;
-    } else {
-      uint32_t part = 0;
-      for (int i = tid; i <= static_cast<int>(mask); i += kThreads)
-        part += static_cast<uint32_t>(i) > sel.t ? hist[hist_index(i)] : 0u;
-      tie_local = hist[hist_index(static_cast<int>(sel.t))];
-      above_local += block_sum(part, ctl);
-    }
-    need -= sel.above;
-    prefix = (prefix << w) | sel.t;
-    shift = nshift;
-    cnt = sel.count;
-    if (cnt <= cap || shift == 0) break;
-  }
-
-  const uint32_t k_above = static_cast<uint32_t>(k) - need;  // winners above the bin
-  uint32_t win_base = 0, tie_base = 0;
-  if (G > 1) {
-    if (tid < G) {
-      dsmem_st(map_rank(smem_addr(&ctl.xa[rank]), tid), above_local);
-      dsmem_st(map_rank(smem_addr(&ctl.xt[rank]), tid), tie_local);
-    }
-    cluster_sync();
-    for (int r = 0; r < rank; ++r) {
-      win_base += ctl.xa[r];
-      tie_base += ctl.xt[r];
-    }
-  }
-
-  if (cnt <= cap) {
-    const bool remote = G > 1 && rank != 0;
-    const uint32_t ties_remote = G > 1 ? map_rank(smem_addr(buf), 0) : 0u;
-    scatter_pass<F>(s, prefix, shift, out, k, win_base, tie_base, buf, ties_remote, remote, cap, m,
-                    ctl);
-    if (G > 1)
-      cluster_sync();  // CTA 0 now holds every tie
-    else
-      __syncthreads();
-    if (rank == 0)
-      select_in_buffer<F>(buf, cnt, need, prefix, 32 + shift, L, out, k, k_above, m, hist, ctl);
-  } else {
-    // tie_base is this CTA's first position among the elements equal to prefix
-    const uint32_t quota = tie_base >= need ? 0u : min(need - tie_base, tie_local);
-    const uint32_t eq_slot0 = k_above + min(tie_base, need);
-    emit_equal<F>(s, prefix, out, k, win_base, eq_slot0, quota, m, ctl);
-  }
+  exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl);
 }
 
 // One cluster of G CTAs per row (with kSingle: one CTA, G = 1 at compile time).
@@ -1673,7 +2275,9 @@ template <int F>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_rows_kernel(const Params p) {
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Ctl ctl;
-  if constexpr ((F & kSingle) != 0) {
+  if constexpr ((F & kStaged) != 0) {
+    staged_row<F>(p, static_cast<int>(blockIdx.x), dyn, ctl);
+  } else if constexpr ((F & kSingle) != 0) {
     row_body<F>(p, static_cast<int>(blockIdx.x), 1, 0, dyn, ctl);
   } else {
     const int G = static_cast<int>(cluster_nctarank());
@@ -1697,7 +2301,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   while (i + 1 < gp.n && gp.row_begin[i + 1] <= item) ++i;
   if (threadIdx.x == 0) prob = gp.probs[i];
   __syncthreads();
-  row_body<F>(prob, item - gp.row_begin[i], G, static_cast<int>(cluster_ctarank()), dyn, ctl);
+  if constexpr ((F & kStaged) != 0)
+    staged_row<F>(prob, item - gp.row_begin[i], dyn, ctl);
+  else
+    row_body<F>(prob, item - gp.row_begin[i], G, static_cast<int>(cluster_ctarank()), dyn, ctl);
 }
 
 // The sort pass of the sorted output (one CTA per row, after the selection kernel):
@@ -1770,13 +2377,40 @@ __global__ void __launch_bounds__(kThreads) topk_sort_kernel(const Params p) {
   }
 }
 
-template <class Kernel, class Arg>
+// Dynamic shared memory of a launch: the rows kernels' layout for clusters of g, or
+// the staged tier's.
+constexpr size_t rows_smem_bytes(int g, int tie_cap) {
+  return sizeof(uint32_t) * static_cast<size_t>(kHistWords * (g > 1 ? 2 : 1) + kListWords + kPtCap) +
+         sizeof(uint2) * static_cast<size_t>(tie_cap);
+}
+template <bool kHalf>
+constexpr size_t staged_smem_bytes(int tie_cap) {
+  return sizeof(uint32_t) * static_cast<size_t>(staged_fixed_words<kHalf>()) +
+         sizeof(uint2) * static_cast<size_t>(tie_cap);
+}
+
+#ifdef TOPK_FORM
+// ---------------------------------------------------------------- one form's kernels
+//
+// Each form's kernels are compiled in an object of their own (TOPK_FORM = the form),
+// so that the objects build in parallel; the object without TOPK_FORM holds the
+// dispatch by form below.
+
+// Dynamic shared memory of a kernel with template argument F.
+template <int F>
+constexpr size_t kernel_smem_bytes(int g, int tie_cap) {
+  return (F & kStaged) == 0        ? rows_smem_bytes(g, tie_cap)
+         : (F & kHalfStage) != 0   ? staged_smem_bytes<true>(tie_cap)
+                                   : staged_smem_bytes<false>(tie_cap);
+}
+
+template <int F, class Kernel, class Arg>
 cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, int tie_cap,
                             cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(rows * g), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(g, tie_cap);
+  cfg.dynamicSmemBytes = kernel_smem_bytes<F>(g, tie_cap);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1791,66 +2425,97 @@ cudaError_t launch_clusters(Kernel kernel, const Arg& arg, int64_t rows, int g, 
 }
 
 template <int F>
-cudaError_t launch_form(const Params& p, int g, bool keys_in_filter, cudaStream_t stream) {
-  if (g == 1 && keys_in_filter)
-    return launch_clusters(topk_rows_kernel<F | kSingle | kKeysInFilter>, p, p.batch, 1,
-                           p.tie_cap, stream);
-  if (g == 1) return launch_clusters(topk_rows_kernel<F | kSingle>, p, p.batch, 1, p.tie_cap, stream);
-  return launch_clusters(topk_rows_kernel<F>, p, p.batch, g, p.tie_cap, stream);
+cudaError_t launch_group_form(const GroupParams& gp, int g, cudaStream_t stream) {
+  return launch_clusters<F>(topk_group_kernel<F>, gp, gp.row_begin[gp.n], g, gp.probs[0].tie_cap,
+                            stream);
 }
 
 template <int F>
-cudaError_t launch_group_form(const GroupParams& gp, int g, cudaStream_t stream) {
-  return launch_clusters(topk_group_kernel<F>, gp, gp.row_begin[gp.n], g, gp.probs[0].tie_cap,
-                         stream);
+cudaError_t launch_rows_form(const Params& p, int g, cudaStream_t stream) {
+  return launch_clusters<F>(topk_rows_kernel<F>, p, p.batch, g, p.tie_cap, stream);
 }
 
 template <class Kernel>
-cudaError_t prepare_kernel(Kernel kernel) {
+cudaError_t prepare_kernel(Kernel kernel, size_t smem = rows_smem_bytes(2, kTieCapMax)) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes(2, kTieCapMax)));
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int F>
-cudaError_t prepare_form() {
+constexpr int kForm = TOPK_FORM;
+static_assert(kForm >= kRaw && kForm <= kWindow, "TOPK_FORM must be a Form");
+
+}  // namespace
+
+#if TOPK_FORM == 0
+#define TOPK_FORM_NS raw
+#elif TOPK_FORM == 1
+#define TOPK_FORM_NS paged
+#elif TOPK_FORM == 2
+#define TOPK_FORM_NS ragged
+#else
+#define TOPK_FORM_NS window
+#endif
+
+namespace TOPK_FORM_NS {
+
+cudaError_t prepare_device() {
+  constexpr int F = kForm;
   cudaError_t e = prepare_kernel(topk_rows_kernel<F>);
   if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle>);
   if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts | kKeysInFilter>);
-  return e == cudaSuccess ? prepare_kernel(topk_group_kernel<F | kOpts>) : e;
-}
-
-}  // namespace
-
-size_t smem_bytes(int g, int tie_cap) {
-  return sizeof(uint32_t) * (kHistWords * (g > 1 ? 2 : 1) + kListWords + kPtCap) +
-         sizeof(uint2) * static_cast<size_t>(tie_cap);
-}
-
-cudaError_t prepare_device() {
-  cudaError_t e = prepare_form<kRaw>();
-  if (e == cudaSuccess) e = prepare_form<kPaged>();
-  if (e == cudaSuccess) e = prepare_form<kRagged>();
-  if (e == cudaSuccess) e = prepare_form<kWindow>();
+  if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts>);
+  if constexpr (kHasStaged) {
+    const size_t full = staged_smem_bytes<false>(kTieCapMax), half = staged_smem_bytes<true>(kTieCapMax);
+    if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kStaged>, full);
+    if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kStaged>, full);
+    if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts | kStaged>, full);
+    if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kStaged | kHalfStage>, half);
+    if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kStaged | kHalfStage>, half);
+    if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts | kStaged | kHalfStage>, half);
+  }
   return e;
 }
 
-cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter, cudaStream_t stream) {
-  switch (form) {
-    case kRaw: return launch_form<kRaw>(p, g, keys_in_filter, stream);
-    case kPaged: return launch_form<kPaged>(p, g, keys_in_filter, stream);
-    case kRagged: return launch_form<kRagged>(p, g, keys_in_filter, stream);
-    case kWindow: return launch_form<kWindow>(p, g, keys_in_filter, stream);
+cudaError_t launch(const Params& p, int g, bool keys_in_filter, int staged, cudaStream_t stream) {
+  constexpr int F = kForm;
+  if constexpr (kHasStaged) {
+    if (g == 1 && staged == 1) return launch_rows_form<F | kSingle | kStaged>(p, 1, stream);
+    if (g == 1 && staged == 2) return launch_rows_form<F | kSingle | kStaged | kHalfStage>(p, 1, stream);
+  } else {
+    if (staged != 0) return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
+  if (g == 1 && keys_in_filter) return launch_rows_form<F | kSingle | kKeysInFilter>(p, 1, stream);
+  if (g == 1) return launch_rows_form<F | kSingle>(p, 1, stream);
+  return launch_rows_form<F>(p, g, stream);
 }
 
-template <int F>
-cudaError_t sort_form(const Params& p, cudaStream_t stream) {
+cudaError_t launch_group(const GroupParams& gp, int g, bool opts, bool keys_in_filter, int staged,
+                         cudaStream_t stream) {
+  constexpr int F = kForm;
+  if constexpr (kHasStaged) {
+    if (staged == 1 && g == 1)
+      return opts ? launch_group_form<F | kOpts | kStaged>(gp, g, stream)
+                  : launch_group_form<F | kStaged>(gp, g, stream);
+    if (staged == 2 && g == 1)
+      return opts ? launch_group_form<F | kOpts | kStaged | kHalfStage>(gp, g, stream)
+                  : launch_group_form<F | kStaged | kHalfStage>(gp, g, stream);
+  } else {
+    if (staged != 0) return cudaErrorInvalidValue;
+  }
+  const bool keys = keys_in_filter && g == 1;
+  if (opts)
+    return keys ? launch_group_form<F | kOpts | kKeysInFilter>(gp, g, stream)
+                : launch_group_form<F | kOpts>(gp, g, stream);
+  return keys ? launch_group_form<F | kKeysInFilter>(gp, g, stream)
+              : launch_group_form<F>(gp, g, stream);
+}
+
+cudaError_t sort_rows(const Params& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1860,7 +2525,7 @@ cudaError_t sort_form(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_sort_kernel<F>, p);
+  return cudaLaunchKernelEx(&cfg, topk_sort_kernel<kForm | kOpts>, p);
 }
 
 cudaError_t guard_hits(unsigned int* hits) {
@@ -1872,36 +2537,79 @@ cudaError_t reset_guard_hits() {
   return cudaMemcpyToSymbol(g_guard_hits, &zero, sizeof(unsigned int));
 }
 
-cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {
-  switch (form) {
-    case kRaw: return sort_form<kRaw | kOpts>(p, stream);
-    case kPaged: return sort_form<kPaged | kOpts>(p, stream);
-    case kRagged: return sort_form<kRagged | kOpts>(p, stream);
-    case kWindow: return sort_form<kWindow | kOpts>(p, stream);
-  }
-  return cudaErrorInvalidValue;
+}  // namespace TOPK_FORM_NS
+#undef TOPK_FORM_NS
+
+#else
+// ---------------------------------------------------------------- dispatch by form
+
+}  // namespace
+
+size_t smem_bytes(int g, int tie_cap) { return rows_smem_bytes(g, tie_cap); }
+
+bool staged_fits(int64_t row_len) {
+  return kHasStaged && row_len > 0 && row_len <= 4 * static_cast<int64_t>(kStagedQuads);
 }
 
-template <int Bits>
-cudaError_t launch_group_bits(Form form, const GroupParams& gp, int g, cudaStream_t stream) {
+cudaError_t prepare_device() {
+  cudaError_t e = raw::prepare_device();
+  if (e == cudaSuccess) e = paged::prepare_device();
+  if (e == cudaSuccess) e = ragged::prepare_device();
+  if (e == cudaSuccess) e = window::prepare_device();
+  return e;
+}
+
+cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter, int staged,
+                   cudaStream_t stream) {
   switch (form) {
-    case kRaw: return launch_group_form<kRaw | Bits>(gp, g, stream);
-    case kPaged: return launch_group_form<kPaged | Bits>(gp, g, stream);
-    case kRagged: return launch_group_form<kRagged | Bits>(gp, g, stream);
-    case kWindow: return launch_group_form<kWindow | Bits>(gp, g, stream);
+    case kRaw: return raw::launch(p, g, keys_in_filter, staged, stream);
+    case kPaged: return paged::launch(p, g, keys_in_filter, staged, stream);
+    case kRagged: return ragged::launch(p, g, keys_in_filter, staged, stream);
+    case kWindow: return window::launch(p, g, keys_in_filter, staged, stream);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,
-                         bool keys_in_filter, cudaStream_t stream) {
-  const bool keys = keys_in_filter && g == 1;
-  if (opts)
-    return keys ? launch_group_bits<kOpts | kKeysInFilter>(form, gp, g, stream)
-                : launch_group_bits<kOpts>(form, gp, g, stream);
-  return keys ? launch_group_bits<kKeysInFilter>(form, gp, g, stream)
-              : launch_group_bits<0>(form, gp, g, stream);
+                         bool keys_in_filter, int staged, cudaStream_t stream) {
+  switch (form) {
+    case kRaw: return raw::launch_group(gp, g, opts, keys_in_filter, staged, stream);
+    case kPaged: return paged::launch_group(gp, g, opts, keys_in_filter, staged, stream);
+    case kRagged: return ragged::launch_group(gp, g, opts, keys_in_filter, staged, stream);
+    case kWindow: return window::launch_group(gp, g, opts, keys_in_filter, staged, stream);
+  }
+  return cudaErrorInvalidValue;
 }
+
+cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {
+  switch (form) {
+    case kRaw: return raw::sort_rows(p, stream);
+    case kPaged: return paged::sort_rows(p, stream);
+    case kRagged: return ragged::sort_rows(p, stream);
+    case kWindow: return window::sort_rows(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t guard_hits(unsigned int* hits) {
+  unsigned int a = 0, b = 0, c = 0, d = 0;
+  cudaError_t e = raw::guard_hits(&a);
+  if (e == cudaSuccess) e = paged::guard_hits(&b);
+  if (e == cudaSuccess) e = ragged::guard_hits(&c);
+  if (e == cudaSuccess) e = window::guard_hits(&d);
+  *hits = a + b + c + d;
+  return e;
+}
+
+cudaError_t reset_guard_hits() {
+  cudaError_t e = raw::reset_guard_hits();
+  if (e == cudaSuccess) e = paged::reset_guard_hits();
+  if (e == cudaSuccess) e = ragged::reset_guard_hits();
+  if (e == cudaSuccess) e = window::reset_guard_hits();
+  return e;
+}
+
+#endif  // TOPK_FORM
 
 }  // namespace TOPK_CTA_NS
 }  // namespace topk_gb300

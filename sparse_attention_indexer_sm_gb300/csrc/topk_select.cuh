@@ -43,9 +43,9 @@ struct GroupParams {
   Params probs[kMaxGroup];
 };
 
-// The kernels are built twice (topk_select.cu): cta512 has 512-thread CTAs, two per
-// SM; cta256 has 256-thread CTAs, four per SM, and takes tie capacities up to
-// kTieCap256 only. Each build exports the same functions.
+// The kernels are built for two CTA sizes (topk_select.cu): cta512 has 512-thread
+// CTAs, two per SM; cta256 has 256-thread CTAs, four per SM, and takes tie
+// capacities up to kTieCap256 only. Each build exports the same functions.
 constexpr int kTieCap256 = 3072;
 
 #define TOPK_CTA_INTERFACE                                                              \
@@ -54,15 +54,20 @@ constexpr int kTieCap256 = 3072;
   /* One-time per-device function attributes (max dynamic smem, cluster size 16). */    \
   cudaError_t prepare_device();                                                         \
   /* Enqueue the kernel: grid = batch * g CTAs in clusters of g along x. With g = 1, */  \
-  /* keys_in_filter picks the variant that reads candidates back from L1 in the */     \
+  /* staged = 1 (whole row staged, one CTA per SM) or 2 (half a row, two per SM) */     \
+  /* picks the staged tier (rows for which staged_fits holds; p.use_filter set), */     \
+  /* else keys_in_filter the variant that reads candidates back from L1 in the */       \
   /* filter (faster once SMs hold two CTAs each). */                                    \
-  cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter,            \
+  cudaError_t launch(Form form, const Params& p, int g, bool keys_in_filter, int staged, \
                      cudaStream_t stream);                                              \
+  /* Whether rows of at most row_len elements (0: unknown) can run on this build's */  \
+  /* staged tier (whole row copied to shared memory; the 512-thread build only). */    \
+  bool staged_fits(int64_t row_len);                                                   \
   /* Enqueue one launch over every row of the group's problems (all of `form`, with */  \
   /* one tie capacity): grid = row_begin[n] * g CTAs in clusters of g. opts: some */    \
   /* problem has the values output or the sorted option (staged). */                    \
   cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,          \
-                           bool keys_in_filter, cudaStream_t stream);                   \
+                           bool keys_in_filter, int staged, cudaStream_t stream);       \
   /* The sort pass of the sorted output: p.staged (filled by a launch with p) is */     \
   /* ordered per row and written to p.out and p.values; one CTA per row. */             \
   cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);                \
@@ -71,12 +76,33 @@ constexpr int kTieCap256 = 3072;
   cudaError_t guard_hits(unsigned int* hits);                                           \
   cudaError_t reset_guard_hits();
 
+// The same calls for one form, each in an object of its own (the calls above
+// dispatch to these).
+#define TOPK_FORM_INTERFACE                                                             \
+  cudaError_t prepare_device();                                                         \
+  cudaError_t launch(const Params& p, int g, bool keys_in_filter, int staged,           \
+                     cudaStream_t stream);                                              \
+  cudaError_t launch_group(const GroupParams& gp, int g, bool opts, bool keys_in_filter, \
+                           int staged, cudaStream_t stream);                            \
+  cudaError_t sort_rows(const Params& p, cudaStream_t stream);                          \
+  cudaError_t guard_hits(unsigned int* hits);                                           \
+  cudaError_t reset_guard_hits();
+
 namespace cta512 {
 TOPK_CTA_INTERFACE
+namespace raw { TOPK_FORM_INTERFACE }
+namespace paged { TOPK_FORM_INTERFACE }
+namespace ragged { TOPK_FORM_INTERFACE }
+namespace window { TOPK_FORM_INTERFACE }
 }
 namespace cta256 {
 TOPK_CTA_INTERFACE
+namespace raw { TOPK_FORM_INTERFACE }
+namespace paged { TOPK_FORM_INTERFACE }
+namespace ragged { TOPK_FORM_INTERFACE }
+namespace window { TOPK_FORM_INTERFACE }
 }
 #undef TOPK_CTA_INTERFACE
+#undef TOPK_FORM_INTERFACE
 
 }  // namespace topk_gb300

@@ -39,14 +39,17 @@ def no_guard_hits(pkg):
 
 
 @contextlib.contextmanager
-def settings(pkg, split=None, tie_cap=None, fast=None, cta=None):
+def settings(pkg, split=None, tie_cap=None, fast=None, cta=None, staged=None):
     prev_split = pkg.topk_set_row_split(split) if split is not None else None
     prev_cap = pkg.topk_set_tie_capacity(tie_cap) if tie_cap is not None else None
     prev_fast = pkg.topk_set_fast_tier(fast) if fast is not None else None
     prev_cta = pkg.topk_set_cta_threads(cta) if cta is not None else None
+    prev_staged = pkg.topk_set_staged_tier(staged) if staged is not None else None
     try:
         yield
     finally:
+        if staged is not None:
+            pkg.topk_set_staged_tier(prev_staged)
         if cta is not None:
             pkg.topk_set_cta_threads(prev_cta)
         if split is not None:
@@ -206,6 +209,87 @@ def test_tie_buffer_capacity(pkg, tie_cap, split, dist, fast):
     with settings(pkg, split=split, tie_cap=tie_cap, fast=fast):
         got = run_gpu(pkg, w)
     assert_parity(w, got)
+
+
+@pytest.mark.parametrize("staged", [2, 3, 0])
+@pytest.mark.parametrize("tie_cap", [0, 16, 300, 4096])
+@pytest.mark.parametrize("dist", ["normal", "decode", "banded", "narrow", "subnormal", "heavy_tail"])
+def test_single_cta_tiers(pkg, dist, tie_cap, staged):
+    """Rows owned by one CTA on the staged tier (the row copied to shared memory from
+    kernel start, whole or by halves) and on the streaming fast tier, with every
+    buffer size down to none (the exact-tier fallback inside each)."""
+    w = _mixed(900 + tie_cap, dist, k=1024 if tie_cap != 300 else 2048)
+    with settings(pkg, split=1, tie_cap=tie_cap, staged=staged):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("staged", [2, 3, 0])
+@pytest.mark.parametrize("form", ["raw", "paged"])
+@pytest.mark.parametrize("batch", [64, 256])
+def test_decode_sweep_both_single_cta_tiers(pkg, batch, form, staged):
+    """The decode sweep on both single-CTA tiers (the streaming tier reads candidates
+    back from L2 below one row per SM and from L1 above)."""
+    w = workloads.config3(batch, form)
+    with settings(pkg, staged=staged):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got, check_rows=8)
+
+
+@pytest.mark.parametrize("staged", [2, 3])
+@pytest.mark.parametrize("stride", [1, 3, 4, 5, 127, 1025, 4097, 8191, 30001, 32764, 32767, 32768])
+def test_staged_tier_strides(pkg, stride, staged):
+    """Row strides of every alignment up to the staged tier's limit, with lengths from
+    zero to the stride (unaligned heads and tails, partial runs and bands)."""
+    g = workloads.rng(1300 + stride)
+    batch, k = 9, 700
+    scores = workloads.random_rows(g, batch, stride, "decode", dup=True)
+    seq = np.array([stride, stride - 1, stride // 2, k, k + 1, 4097, 0, -5, 1], np.int32)
+    seq = np.minimum(seq, stride)
+    pt = workloads.permuted_page_table(g, batch, workloads.pages_for(stride, 16))
+    for form in ("raw", "paged"):
+        w = workloads.Workload(f"staged_stride{stride}_{form}", form, k, scores, seq,
+                               pt if form == "paged" else None, 16)
+        with settings(pkg, staged=staged):
+            got = run_gpu(pkg, w)
+        assert_parity(w, got)
+
+
+@pytest.mark.parametrize("staged", [2, 3])
+def test_staged_tier_short_hint_falls_back(pkg, staged):
+    """Ragged rows longer than their length hint promised: the staged tier cannot hold
+    them and runs the exact tier instead."""
+    g = workloads.rng(1400)
+    lens = np.array([40000, 33000, 32768, 12000, 0, 70000], np.int32)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32) + 3
+    flat = workloads.random_rows(g, 1, int(starts[-1] + lens[-1] + 5), "decode")[0]
+    w = workloads.Workload("ragged_short_hint", "ragged", 1024, flat, lens, None, 64,
+                           row_starts=starts)
+    dev = torch.device("cuda:0")
+    out = torch.full((w.batch, w.k), -7, dtype=torch.int32, device=dev)
+    with settings(pkg, staged=staged):
+        pkg.topk_transform_ragged(torch.from_numpy(flat).to(dev), torch.from_numpy(starts).to(dev),
+                                  torch.from_numpy(lens).to(dev), w.k, max_row_len_hint=20000,
+                                  out=out)
+        torch.cuda.synchronize()
+    assert_parity(w, out.cpu().numpy())
+
+
+@pytest.mark.parametrize("staged", [2, 3])
+def test_staged_tier_forms(pkg, staged):
+    """Ragged and window rows on the staged tier (their data start comes with the
+    length), including windows that start and end anywhere in the row."""
+    g = workloads.rng(1500 + staged)
+    lens = np.array([30000, 5000, 32768, 1024, 0, 9000, 17], np.int32)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32) + 1
+    flat = workloads.random_rows(g, 1, int(starts[-1] + lens[-1] + 3), "decode", dup=True)[0]
+    rag = workloads.Workload("staged_ragged", "ragged", 1000, flat, lens, None, 64, row_starts=starts)
+    win = workloads.prefill_windows(40, 32768, window=20000, k=1000)
+    with settings(pkg, staged=staged):
+        got_r = run_gpu(pkg, rag)
+        got_w = run_gpu(pkg, win)
+    assert_parity(rag, got_r)
+    assert_parity(win, got_w)
 
 
 @pytest.mark.parametrize("split", [1, 2, 8])
@@ -667,6 +751,17 @@ def option_workloads():
 def test_values_and_sorted_output(pkg, sorted_):
     ws = option_workloads()
     for w, (got, vals) in zip(ws, run_options(pkg, ws, sorted_)):
+        assert_options(w, got, vals, sorted_)
+
+
+@pytest.mark.parametrize("staged", [2, 3])
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_values_and_sorted_output_staged(pkg, sorted_, staged):
+    """The options (values, rank order) through grouped launches on the staged tier."""
+    ws = option_workloads()
+    with settings(pkg, staged=staged):
+        outs = run_options(pkg, ws, sorted_)
+    for w, (got, vals) in zip(ws, outs):
         assert_options(w, got, vals, sorted_)
 
 
