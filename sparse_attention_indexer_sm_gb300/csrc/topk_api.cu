@@ -239,6 +239,7 @@ size_t staging_bytes(const topk_problem_t* problems, int32_t n, size_t* offsets)
 int check_group(const topk_problem_t* problems, int32_t n_problems, Params* params,
                 int64_t* hints, int64_t* rows_of_form) {
   static_assert(TOPK_MAX_GROUP <= topk_gb300::kMaxGroup, "group limit");
+  static_assert(TOPK_MAX_K == topk_gb300::kMaxK, "largest k");
   if (n_problems < 0 || n_problems > TOPK_MAX_GROUP) return TOPK_ERR_INVALID_ARGUMENT;
   if (n_problems > 0 && problems == nullptr) return TOPK_ERR_INVALID_ARGUMENT;
   for (int i = 0; i < n_problems; ++i) {

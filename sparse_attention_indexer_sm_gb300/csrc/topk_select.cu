@@ -127,6 +127,7 @@ constexpr int kCandBits = 11;
 constexpr int kCandBins = 1 << kCandBits;
 constexpr int kCandWords = hist_index(kCandBins);
 static_assert(kHC + kCandWords <= kHistWords, "fast-tier histograms must fit the histogram region");
+static_assert(kHC >= kMaxK, "a row's output slots fit below the candidate histogram");
 
 struct Ctl {
   uint32_t scan[kWarps];              // per-warp partials of block scans
@@ -136,15 +137,13 @@ struct Ctl {
   uint32_t n_cand;                    // cand_cnt of CTA 0, broadcast
   uint32_t sel2_t, sel2_above, sel2_count;  // second threshold of find_threshold2
   uint32_t ns;                        // valid sample size (CTA 0)
-  uint32_t cls_cnt;                   // (winners, ties) slots of the candidate classification
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t sup[32];                   // super-bin sums of the histogram being searched
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
   uint32_t xt[kMaxCluster];           // per-CTA threshold-bin elements
   // staged tier
-  uint32_t wmax[kWarps], wmin[kWarps], wcnt[kWarps];  // per-warp sample extremes and size
-  uint32_t lam_lo, lam_hi, refine;    // the second sample round's window, and whether it runs
+  uint32_t wmax[kWarps], wmin[kWarps], wcnt[kWarps];  // per-warp sample extremes and sizes
 };
 
 struct Sel {
@@ -389,127 +388,50 @@ __device__ __forceinline__ void find_threshold(const uint32_t* h, int nbins, uin
   __syncthreads();
 }
 
-// Every warp of the CTA (a barrier at the end): the sums of the 32 super-bins of S
-// consecutive bins of the padded histogram h (32 S bins) into ctl.sup. A warp that
-// then searches h reads one word per lane instead of S: a lone warp's dependent
-// shared loads cost several thousand cycles at S = 32 or 64 (measured).
-template <int S>
-__device__ __forceinline__ void super_sums(const uint32_t* h, Ctl& ctl) {
-  constexpr int kPer = 32 / kWarps;  // super-bins per warp
-  static_assert(kPer * kWarps == 32 && S % 32 == 0, "super-bins split evenly");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Every thread of the CTA: in the padded histogram h of kThreads * P bins, the bin
+// where the count from the top reaches need1 (-> ctl.sel_*) and, if `two`, need2
+// (-> ctl.sel2_*); a need outside [1, sum of h] finds nothing. Thread t holds bins
+// [P t, P t + P): a suffix scan over the warp's lanes, one barrier for the warps'
+// totals, and each thread checks its own bins. The results are visible after the
+// caller's next barrier; ctl.scan is written. (A lone warp searching the whole
+// histogram measured several times slower: its dependent shared loads, shuffles
+// and branches do not overlap with any other warp's.)
+template <int P>
+__device__ __forceinline__ void block_find2(const uint32_t* h, uint32_t need1, uint32_t need2,
+                                            bool two, Ctl& ctl) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t c[P];
+  uint32_t s = 0;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int sb = warp * kPer + j;
-    uint32_t a = 0;
-#pragma unroll
-    for (int i = 0; i < S / 32; ++i) a += h[hist_index(sb * S + i * 32 + lane)];
-    a = __reduce_add_sync(kFull, a);
-    if (lane == 0) ctl.sup[sb] = a;
+  for (int i = 0; i < P; ++i) {
+    c[i] = h[hist_index(tid * P + i)];
+    s += c[i];
   }
+  uint32_t x = s;  // count in the bins of lanes >= lane
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_down_sync(kFull, x, off);
+    if (lane + off < 32) x += y;
+  }
+  if (lane == 0) ctl.scan[warp] = x;
   __syncthreads();
-}
-
-// One warp (all 32 lanes) finds, in the padded kFastBins-bin histogram h whose
-// super-bin sums (32 bins each) are in ctl.sup, the threshold bin for need1
-// (-> ctl.sel_*) and, if `two`, for need2 (-> ctl.sel2_*): the bin where the count
-// from the top reaches need (1 <= need <= sum of h). A suffix scan over the lanes'
-// super-bins names the super-bin holding each threshold, and the warp then scans
-// its 32 bins, one per lane, for both needs at once. The results are visible to the
-// block after the caller's next barrier.
-__device__ __forceinline__ void warp_find2(const uint32_t* h, uint32_t need1, uint32_t need2,
-                                           bool two, Ctl& ctl) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t s = ctl.sup[lane];  // bins [32 lane, 32 lane + 32)
-  uint32_t x = s;  // count in the bins of lanes >= lane
+  // the count in higher warps' bins: lane w < kWarps reads warp w's total
+  uint32_t a = __reduce_add_sync(kFull, lane < kWarps && lane > warp ? ctl.scan[lane] : 0u) + x - s;
+  const uint32_t n2 = two ? need2 : 0u;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_down_sync(kFull, x, off);
-    if (lane + off < 32) x += y;
-  }
-  const uint32_t excl = x - s;  // count in the bins of lanes > lane
-  // both searches in the same instructions (their latencies overlap)
-  const uint32_t n2 = two ? need2 : need1;
-  const uint32_t hit1 = __ballot_sync(kFull, s != 0 && excl < need1 && need1 <= x);
-  const uint32_t hit2 = __ballot_sync(kFull, s != 0 && excl < n2 && n2 <= x);
-  // (a need outside [1, sum] finds nothing: no lane writes below; no early exit, as a
-  // lone warp pays an instruction fetch at every taken branch)
-  const int o1 = max(__ffs(hit1) - 1, 0), o2 = max(__ffs(hit2) - 1, 0);
-  const uint32_t above1 = __shfl_sync(kFull, excl, o1), above2 = __shfl_sync(kFull, excl, o2);
-  const int b1 = o1 * 32 + lane, b2 = o2 * 32 + lane;
-  const uint32_t c1 = h[hist_index(b1)], c2 = h[hist_index(b2)];
-  uint32_t y1 = c1, y2 = c2;  // counts in the owner's bins >= b
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t z1 = __shfl_down_sync(kFull, y1, off);
-    const uint32_t z2 = __shfl_down_sync(kFull, y2, off);
-    if (lane + off < 32) {
-      y1 += z1;
-      y2 += z2;
+  for (int i = P - 1; i >= 0; --i) {
+    const uint32_t b = static_cast<uint32_t>(tid * P + i);
+    if (a < need1 && need1 <= a + c[i]) {
+      ctl.sel_t = b;
+      ctl.sel_above = a;
+      ctl.sel_count = c[i];
     }
-  }
-  const uint32_t a1 = above1 + y1 - c1, a2 = above2 + y2 - c2;
-  const uint32_t here1 = __ballot_sync(kFull, c1 != 0 && a1 < need1 && need1 <= a1 + c1);
-  const uint32_t here2 = __ballot_sync(kFull, c2 != 0 && a2 < n2 && n2 <= a2 + c2);
-  const bool w1 = hit1 != 0u && here1 != 0u && lane == __ffs(here1) - 1;
-  const bool w2 = two && hit2 != 0u && here2 != 0u && lane == __ffs(here2) - 1;
-  if (w1) {
-    ctl.sel_t = static_cast<uint32_t>(b1);
-    ctl.sel_above = a1;
-    ctl.sel_count = c1;
-  }
-  if (w2) {
-    ctl.sel2_t = static_cast<uint32_t>(b2);
-    ctl.sel2_above = a2;
-    ctl.sel2_count = c2;
-  }
-}
-
-// One warp (all 32 lanes) finds, in the padded kCandBins-bin candidate histogram h
-// whose super-bin sums (P = kCandBins / 32 bins each) are in ctl.sup, the bin where
-// the count from the top reaches need (1 <= need <= sum of h) and writes it to
-// ctl.sel_* (visible to the block after the caller's next barrier): a suffix scan
-// over the lanes' super-bins names the one holding the threshold; then each lane
-// takes P / 32 of its bins.
-__device__ __forceinline__ void warp_find_cand(const uint32_t* h, uint32_t need, Ctl& ctl) {
-  constexpr int P = kCandBins / 32;  // bins of a super-bin
-  constexpr int P2 = P / 32;         // bins per lane in the second step
-  const int lane = threadIdx.x & 31;
-  const uint32_t s = ctl.sup[lane];  // bins [P lane, P lane + P)
-  uint32_t x = s;  // count in the bins of lanes >= lane
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_down_sync(kFull, x, off);
-    if (lane + off < 32) x += y;
-  }
-  const uint32_t hit = __ballot_sync(kFull, s != 0 && x - s < need && need <= x);
-  // (need outside [1, sum] finds nothing: no lane writes below; straight-line code,
-  // as a lone warp pays an instruction fetch at every taken branch)
-  const int o = max(__ffs(hit) - 1, 0);
-  const uint32_t above = __shfl_sync(kFull, x - s, o);
-  const int b0 = o * P + lane * P2;  // this lane's bins [b0, b0 + P2) of the owner's range
-  uint32_t c[P2];
-  uint32_t s2 = 0;
-#pragma unroll
-  for (int i = 0; i < P2; ++i) {
-    c[i] = h[hist_index(b0 + i)];
-    s2 += c[i];
-  }
-  uint32_t y = s2;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t z = __shfl_down_sync(kFull, y, off);
-    if (lane + off < 32) y += z;
-  }
-  const uint32_t acc = above + y - s2;  // count above this lane's bins
-  const uint32_t here = __ballot_sync(kFull, s2 != 0 && acc < need && need <= acc + s2);
-  // the owning lane's bin, from the top: the first whose count reaches need
-  static_assert(P2 == 2, "two bins per lane");
-  const bool upper = acc + c[1] >= need;
-  if (hit != 0u && here != 0u && lane == __ffs(here) - 1) {
-    ctl.sel_t = static_cast<uint32_t>(b0 + (upper ? 1 : 0));
-    ctl.sel_above = upper ? acc : acc + c[1];
-    ctl.sel_count = upper ? c[1] : c[0];
+    if (a < n2 && n2 <= a + c[i]) {
+      ctl.sel2_t = b;
+      ctl.sel2_above = a;
+      ctl.sel2_count = c[i];
+    }
+    a += c[i];
   }
 }
 
@@ -816,14 +738,13 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist + kH1, mhist + kH1, kFastWords);
-  // the sample has arrived: now the bulk of the slice, issued by the last warp while
-  // the first one looks for the thresholds
+  // the sample has arrived: now the bulk of the slice, issued by the last warp
+  // before the thresholds are looked for
   if (!prefetched) prefetch_slice(s, kThreads - 32);
-  if (rank == 0) super_sums<32>((G > 1 ? mhist : hist) + kH1, ctl);
   // sample ranks a few standard deviations either side of the expected sample rank
-  // of the row's k-th key
+  // of the row's k-th key; CTA 0 finds their coarse bins
   uint32_t rs = 0, rs_lo = 0;
-  if (finder) {
+  if (rank == 0) {
     const uint32_t ns = ctl.ns;
     if (ns != 0) {
       // four standard deviations on lambda's side (a lambda above the k-th key
@@ -835,13 +756,15 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
           fmaxf(__fdividef(static_cast<float>(k) * static_cast<float>(ns), static_cast<float>(L)),
                 1.0f);
       const float sd = mean * rsqrtf(mean);
-      rs = static_cast<uint32_t>(ceilf(mean + 4.0f * sd)) + 2u;
-      if (rs > ns) rs = ns;
+      rs = min(static_cast<uint32_t>(ceilf(mean + 4.0f * sd)) + 2u, ns);
       const float lo = floorf(mean - 3.0f * sd);
-      rs_lo = lo < 1.0f ? 1u : static_cast<uint32_t>(lo);
-      if (rs_lo > rs) rs_lo = rs;
-      warp_find2((G > 1 ? mhist : hist) + kH1, rs, rs_lo, true, ctl);
+      rs_lo = min(lo < 1.0f ? 1u : static_cast<uint32_t>(lo), rs);
     }
+    block_find2<kFastBins / kThreads>((G > 1 ? mhist : hist) + kH1, rs, rs_lo, ns != 0, ctl);
+    __syncthreads();
+  }
+  if (finder) {
+    const uint32_t ns = ctl.ns;
     __syncwarp();
     if (tid == 0) {
       constexpr int kC = 32 - kFastBits;  // coarse bin width exponent
@@ -884,10 +807,12 @@ __device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice&
   }
   __syncthreads();
   if (G > 1) merge_into_cta0(hist + kH2, mhist + kH2, kFastWords);
-  if (rank == 0) super_sums<32>((G > 1 ? mhist : hist) + kH2, ctl);
+  if (rank == 0) {
+    block_find2<kFastBins / kThreads>((G > 1 ? mhist : hist) + kH2, rs != 0 ? rs - win_above : 0u,
+                                      rs_lo - win_above, rs != 0, ctl);
+    __syncthreads();
+  }
   if (finder) {
-    if (rs != 0)
-      warp_find2((G > 1 ? mhist : hist) + kH2, rs - win_above, rs_lo - win_above, true, ctl);
     __syncwarp();
     if (tid == 0) {
       if (rs != 0) {
@@ -1206,58 +1131,98 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
   }
 }
 
+// The k selected positions of a row, staged in shared memory slot by slot (slots
+// [0, upto)), written to out at once: coalesced stores from every thread, and one
+// copy of the mapping code. A slot holding no position of the row (possible only
+// when the scores changed while the kernel ran) is written as -1.
+template <int F>
+__device__ __forceinline__ void write_slots(const int32_t* slots, uint32_t upto, int32_t L,
+                                            int32_t* out, const OutMap& m) {
+  for (uint32_t i = threadIdx.x; i < upto; i += kThreads) {
+    const int32_t j = slots[i];
+    out[i] = static_cast<uint32_t>(j) < static_cast<uint32_t>(L) ? map_pos<F>(m, j) : -1;
+  }
+}
+
 // F3 (CTA 0 only): the filter left n candidates in buf and their histogram (bin =
 // min((key - lambda) >> shift, kCandBins - 1)) in chist. Writes the k largest composites
 // (key, ~position) mapped to out. h may be chist itself: it is used only after
-// chist has been read.
+// chist has been read. Launches without the values or sorted outputs stage the
+// positions in `slots` (k words of shared memory that may overlap h but nothing
+// else) and write them out at the end; the others emit each slot as it is decided.
 template <int F>
 __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, uint32_t k,
                                                   uint32_t* chist, uint32_t lambda,
                                                   uint32_t shift, uint2* list, uint32_t* h,
-                                                  int32_t L, int32_t* out, const OutMap& m,
-                                                  Ctl& ctl) {
+                                                  int32_t* slots, int32_t L, int32_t* out,
+                                                  const OutMap& m, Ctl& ctl) {
+  constexpr bool kSlots = !opts_of(F);
   const int tid = threadIdx.x;
-  super_sums<kCandBins / 32>(chist, ctl);
-  if (tid < 32) warp_find_cand(chist, k, ctl);
+  // slot s gets position j (key `key`)
+  auto put = [&](uint32_t s, uint2 e) {
+    if constexpr (kSlots)
+      slots[s] = static_cast<int32_t>(e.y);
+    else
+      emit<F>(out, static_cast<int32_t>(k), s, m, static_cast<int32_t>(e.y), e.x);
+  };
+  block_find2<kCandBins / kThreads>(chist, k, 0u, false, ctl);
   __syncthreads();
   const uint32_t t = ctl.sel_t, above = ctl.sel_above, ct = ctl.sel_count;
   if (__builtin_expect(ct > static_cast<uint32_t>(kListCap), 0)) {
     select_in_buffer<F>(buf, n, k, 0ull, 64, L, out, static_cast<int32_t>(k), 0u, m, h, ctl);
     return;
   }
-  // candidates above the threshold bin are winners; the bin's go to the list. The
-  // buffer is taken in warp-uniform rounds of kThreads entries (entry tid of each
-  // round); per round, each warp reserves its winners' and ties' slots at once (one
-  // atomic on the packed pair in ctl.cls_cnt) and each lane writes at its rank among
-  // the warp's, with no branch a lone lane would take.
-  const int lane = tid & 31;
-  for (uint32_t base = 0; base < n; base += kThreads) {
-    const uint32_t i = base + static_cast<uint32_t>(tid);
-    const bool live = i < n;
-    const uint2 e = live ? buf[i] : make_uint2(0u, 0u);
-    const uint32_t b = min((e.x - lambda) >> shift, static_cast<uint32_t>(kCandBins - 1));
-    const bool win = live && b > t, tie = live && b == t;
-    const uint32_t wm = __ballot_sync(kFull, win), tm = __ballot_sync(kFull, tie);
-    uint32_t off = 0;
-    if (lane == 0 && (wm | tm) != 0u)
-      off = atomicAdd(&ctl.cls_cnt, static_cast<uint32_t>(__popc(wm)) |
-                                        (static_cast<uint32_t>(__popc(tm)) << 16));
-    off = __shfl_sync(kFull, off, 0);
-    const uint32_t lt = lanemask_lt();
-    const uint32_t ws = (off & 0xFFFFu) + static_cast<uint32_t>(__popc(wm & lt));
-    const uint32_t ts = (off >> 16) + static_cast<uint32_t>(__popc(tm & lt));
-    if (win) {
-      if (ws < above)
-        emit<F>(out, static_cast<int32_t>(k), ws, m, static_cast<int32_t>(e.y), e.x);
-      else
-        guard_hit();
+  // candidates above the threshold bin are winners; the bin's go to the list. Each
+  // thread classifies up to kClsR entries of the buffer at once (entries base +
+  // r kThreads + tid), held in registers; a block scan of the packed (winners, ties)
+  // counts then gives each thread its first slot of each kind.
+  constexpr int kClsR = 8;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t run = 0;  // (winners, ties) slots taken by the earlier sweeps, packed
+  for (uint32_t base = 0; base < n; base += static_cast<uint32_t>(kClsR * kThreads)) {
+    uint2 e[kClsR];
+    uint32_t wb = 0, tb = 0;
+#pragma unroll
+    for (int r = 0; r < kClsR; ++r) {
+      const uint32_t i = base + static_cast<uint32_t>(r * kThreads + tid);
+      const bool live = i < n;
+      e[r] = live ? buf[i] : make_uint2(0u, 0u);
+      const uint32_t b = min((e[r].x - lambda) >> shift, static_cast<uint32_t>(kCandBins - 1));
+      wb |= static_cast<uint32_t>(live && b > t) << r;
+      tb |= static_cast<uint32_t>(live && b == t) << r;
     }
-    if (tie) {
-      if (ts < ct)
-        list[ts] = e;
-      else
-        guard_hit();
+    // winners number above < k and ties ct <= kListCap: each fits 16 bits
+    const uint32_t mine = static_cast<uint32_t>(__popc(wb)) | (static_cast<uint32_t>(__popc(tb)) << 16);
+    uint32_t x = mine;  // inclusive prefix over the warp's lanes
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, off);
+      if (lane >= off) x += y;
     }
+    if (lane == 31) ctl.scan[warp] = x;
+    __syncthreads();
+    const uint32_t sw = lane < kWarps ? ctl.scan[lane] : 0u;
+    const uint32_t first = run + __reduce_add_sync(kFull, lane < warp ? sw : 0u) + x - mine;
+    run += __reduce_add_sync(kFull, sw);
+    uint32_t ws = first & 0xFFFFu, ts = first >> 16;
+#pragma unroll
+    for (int r = 0; r < kClsR; ++r) {
+      if ((wb >> r) & 1u) {
+        if (ws < above)
+          put(ws, e[r]);
+        else
+          guard_hit();
+        ++ws;
+      }
+      if ((tb >> r) & 1u) {
+        if (ts < ct)
+          list[ts] = e[r];
+        else
+          guard_hit();
+        ++ts;
+      }
+    }
+    if (base + static_cast<uint32_t>(kClsR * kThreads) < n) __syncthreads();  // ctl.scan again
   }
   __syncthreads();
   const uint32_t need = k - above;  // 1 <= need <= ct
@@ -1274,7 +1239,11 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
         const uint2 o = list[j];
         r += before(e, o.x, o.y);
       }
-      if (r < need) emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y), e.x);
+      if (r < need) put(above + r, e);
+    }
+    if constexpr (kSlots) {
+      __syncthreads();
+      write_slots<F>(slots, k, L, out, m);
     }
     return;
   }
@@ -1309,10 +1278,17 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
     }
     if (tid < ((static_cast<int>(ct) * g + 31) & ~31)) {  // whole warps that hold an entry
       for (int off = g >> 1; off > 0; off >>= 1) r += __shfl_xor_sync(kFull, r, off);
-      if (live && part == 0u && r < need)
-        emit<F>(out, static_cast<int32_t>(k), above + r, m, static_cast<int32_t>(e.y), e.x);
+      if (live && part == 0u && r < need) put(above + r, e);
+    }
+    if constexpr (kSlots) {
+      __syncthreads();
+      write_slots<F>(slots, k, L, out, m);
     }
     return;
+  }
+  if constexpr (kSlots) {  // the winners out first: h may overlap the slots
+    write_slots<F>(slots, above, L, out, m);
+    __syncthreads();
   }
   select_in_buffer<F>(list, ct, need, 0ull, 64, L, out, static_cast<int32_t>(k), above, m, h, ctl);
 }
@@ -1579,7 +1555,8 @@ template <bool kHalf>
 __host__ __device__ constexpr int stage_words() { return (kHalf ? kPassChunks : kStagedChunks) * kChunkQuads * 4; }
 template <bool kHalf>
 __host__ __device__ constexpr int staged_fixed_words() { return stage_words<kHalf>() + kFastWords + kCandWords + kPtStaged; }
-static_assert(kListWords + kHistWords <= stage_words<true>(), "list and scratch must fit the staging area");
+static_assert(kListWords + kHistWords + kMaxK <= stage_words<true>(),
+              "list, scratch and output slots must fit the staging area");
 
 
 // 128-bit read-only load issued where it stands (volatile: the compiler may not move
@@ -1723,14 +1700,16 @@ __device__ __forceinline__ void filter_pass(const uint4* stage, int slot0, int c
 }
 
 // The second sample round of staged_lambda (every thread; the same sample quad v at
-// row position j, `in` as there): 1024 equal key bins over [ctl.lam_lo, ctl.lam_hi]
-// (keys above it counted apart) in chist's region, which is cleared again
-// afterwards; ctl.lambda and ctl.lambda_shift are updated. Kept out of line, as it
-// runs only for scores packed into a narrow band.
-__device__ __noinline__ void staged_refine(uint4 v, int32_t j, bool in, int32_t L, uint32_t rs,
-                                           uint32_t rs_lo, uint32_t* chist, Ctl& ctl) {
+// row position j, `in` as there): 1024 equal key bins over [wlo, whi] (keys above
+// it counted apart) in chist's region, which is cleared again afterwards. Returns
+// lambda and sets *shift; when rs falls above the window (rounding), round 1's
+// (wlo, shift1) stands. Kept out of line, as it runs only for scores packed into a
+// narrow band.
+__device__ __noinline__ uint32_t staged_refine(uint4 v, int32_t j, bool in, int32_t L, uint32_t rs,
+                                               uint32_t rs_lo, uint32_t wlo, uint32_t whi,
+                                               uint32_t shift1, uint32_t* chist, Ctl& ctl,
+                                               uint32_t* shift) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t wlo = ctl.lam_lo, whi = ctl.lam_hi;
   const int f = max(0, (32 - __clz(static_cast<int>(whi - wlo))) - kFastBits);
   uint32_t above = 0;
 #pragma unroll
@@ -1743,31 +1722,27 @@ __device__ __noinline__ void staged_refine(uint4 v, int32_t j, bool in, int32_t 
       atomicAdd(&chist[hist_index(static_cast<int>((key - wlo) >> f))], 1u);
   }
   above = __reduce_add_sync(kFull, above);
-  __syncthreads();  // every thread has read ctl.refine and the window
   if (lane == 0) ctl.wcnt[warp] = above;
-  __syncthreads();
+  __syncthreads();  // (also: every thread has read round 1's bins)
   uint32_t na = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) na += ctl.wcnt[w];
-  super_sums<32>(chist, ctl);
-  if (warp == 0 && rs > na) {  // else rs lies above the window (rounding): round 1 stands
-    const bool two = rs_lo > na;
-    warp_find2(chist, rs - na, two ? rs_lo - na : rs - na, two, ctl);
-    __syncwarp();
-    if (lane == 0) {
-      const uint32_t lam = wlo + (ctl.sel_t << f);
-      const uint64_t top =
-          static_cast<uint64_t>(wlo) + (static_cast<uint64_t>(ctl.sel2_t + 1u) << f) - 1u;
-      const uint32_t hi = two ? static_cast<uint32_t>(min(top, static_cast<uint64_t>(whi))) : whi;
-      const uint32_t gap = hi > lam ? hi - lam : 0u;
-      ctl.lambda = lam;
-      ctl.lambda_shift =
-          static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
-    }
-  }
+  const bool go = rs > na, two = rs_lo > na;
+  block_find2<kFastBins / kThreads>(chist, go ? rs - na : 0u, two ? rs_lo - na : 0u, two, ctl);
   __syncthreads();
+  uint32_t lam = wlo, sh = shift1;
+  if (go) {
+    lam = wlo + (ctl.sel_t << f);
+    const uint64_t top =
+        static_cast<uint64_t>(wlo) + (static_cast<uint64_t>(ctl.sel2_t + 1u) << f) - 1u;
+    const uint32_t hi = two ? static_cast<uint32_t>(min(top, static_cast<uint64_t>(whi))) : whi;
+    const uint32_t gap = hi > lam ? hi - lam : 0u;
+    sh = static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
+  }
   for (int i = tid; i < kCandWords; i += kThreads) chist[i] = 0;
   __syncthreads();
+  *shift = sh;
+  return lam;
 }
 
 // Lambda from the sample (every thread of the CTA; thread t holds sample quad v,
@@ -1836,46 +1811,35 @@ __device__ __forceinline__ uint32_t staged_lambda(const uint4& v, int32_t j, boo
     const float lo = floorf(mean - 3.0f * sd);
     rs_lo = min(lo < 1.0f ? 1u : static_cast<uint32_t>(lo), rs);
   }
-  super_sums<32>(shist, ctl);
-  if (warp == 0) {
-    if (usable) warp_find2(shist, rs, rs_lo, true, ctl);
-    __syncwarp();
-    if (lane == 0) {
-      uint32_t refine = 0;
-      if (usable) {
-        // the distances at a window bin's edges (bins 0 and kFastBins - 1 are open)
-        const int32_t bs = kFastBins - 1 - static_cast<int32_t>(ctl.sel_t);
-        const int32_t bl = kFastBins - 1 - static_cast<int32_t>(ctl.sel2_t);
-        const int32_t ehi = bs + base + 1, elo = bl + base;
-        const float dhi = bs >= kFastBins - 1 ? __uint_as_float(0x7F800000u)
-                          : ehi <= 0          ? 0.0f
-                                              : __uint_as_float((static_cast<uint32_t>(ehi) << kDistShift) - 1u);
-        const float dlo = bl <= 0 || elo <= 0 ? 0.0f
-                                              : __uint_as_float(static_cast<uint32_t>(elo) << kDistShift);
-        // keys of M - d, lambda rounded down and lambda_hi up by a few key units
-        const float xlo = Mv - dhi, xhi = Mv - dlo;
-        const uint32_t klo = isnan(xlo) ? 0u : order_key(__float_as_uint(xlo));
-        const uint32_t khi = isnan(xhi) ? M : order_key(__float_as_uint(xhi));
-        const uint32_t lam = klo > 2u ? klo - 2u : 0u;
-        const uint32_t lam_hi = min(khi + 2u < khi ? khi : khi + 2u, M);
-        ctl.lambda = lam;
-        ctl.lam_lo = lam;  // the second round's window: [lam, lam_hi]
-        ctl.lam_hi = lam_hi;
-        refine = ctl.sel_count > kRefineCount && lam_hi > lam ? 1u : 0u;
-        const uint32_t gap = lam_hi > lam ? lam_hi - lam : 0u;
-        ctl.lambda_shift =
-            static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
-      } else {
-        ctl.lambda = 0;
-        ctl.lambda_shift = 32 - kCandBits;
-      }
-      ctl.refine = refine;
-    }
-  }
+  block_find2<kFastBins / kThreads>(shist, rs, rs_lo, usable, ctl);
   __syncthreads();
-  if (__builtin_expect(ctl.refine != 0u, 0)) staged_refine(v, j, in, L, rs, rs_lo, chist, ctl);
-  *shift = ctl.lambda_shift;
-  return ctl.lambda;
+  // every thread: lambda and the candidate-histogram bin width from the bins found
+  if (!usable) {
+    *shift = 32 - kCandBits;
+    return 0u;
+  }
+  // the distances at a window bin's edges (bins 0 and kFastBins - 1 are open)
+  const int32_t bs = kFastBins - 1 - static_cast<int32_t>(ctl.sel_t);
+  const int32_t bl = kFastBins - 1 - static_cast<int32_t>(ctl.sel2_t);
+  const int32_t ehi = bs + base + 1, elo = bl + base;
+  const float dhi = bs >= kFastBins - 1 ? __uint_as_float(0x7F800000u)
+                    : ehi <= 0          ? 0.0f
+                                        : __uint_as_float((static_cast<uint32_t>(ehi) << kDistShift) - 1u);
+  const float dlo = bl <= 0 || elo <= 0 ? 0.0f
+                                        : __uint_as_float(static_cast<uint32_t>(elo) << kDistShift);
+  // keys of M - d, lambda rounded down and lambda_hi up by a few key units
+  const float xlo = Mv - dhi, xhi = Mv - dlo;
+  const uint32_t klo = isnan(xlo) ? 0u : order_key(__float_as_uint(xlo));
+  const uint32_t khi = isnan(xhi) ? M : order_key(__float_as_uint(xhi));
+  const uint32_t lam = klo > 2u ? klo - 2u : 0u;
+  const uint32_t lam_hi = min(khi + 2u < khi ? khi : khi + 2u, M);
+  const uint32_t gap = lam_hi > lam ? lam_hi - lam : 0u;
+  const uint32_t sh =
+      static_cast<uint32_t>(max(0, (32 - __clz(static_cast<int>(gap))) - (kCandBits - 1)));
+  if (__builtin_expect(ctl.sel_count > kRefineCount && lam_hi > lam, 0))
+    return staged_refine(v, j, in, L, rs, rs_lo, lam, lam_hi, sh, chist, ctl, shift);
+  *shift = sh;
+  return lam;
 }
 
 // One row of problem p on the staged tier (one CTA, no cluster).
@@ -1897,7 +1861,6 @@ __device__ __forceinline__ void staged_row(const Params& p, int row, uint32_t* d
     ctl.tie_cnt = 0;
     ctl.out_cnt = 0;
     ctl.cand_cnt = 0;
-    ctl.cls_cnt = 0;
   }
   __syncthreads();  // cleared memory before any use
   wait_prior_grids();
@@ -2069,7 +2032,7 @@ __device__ __forceinline__ void staged_row(const Params& p, int row, uint32_t* d
   uint32_t* scratch = dyn + kListWords;
   if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
     select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list, scratch,
-                         L, out, m, ctl);
+                         reinterpret_cast<int32_t*>(scratch + kHistWords), L, out, m, ctl);
     return;
   }
   // too few (lambda above the k-th key) or too many candidates: exact tier
@@ -2107,7 +2070,6 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     ctl.out_cnt = 0;
     ctl.cand_cnt = 0;
     ctl.ns = 0;
-    ctl.cls_cnt = 0;
     ctl.lambda = 0;
     ctl.lambda_shift = 0;
   }
@@ -2252,7 +2214,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
       if (rank == 0)
         select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
-                             hist, L, out, m, ctl);
+                             hist, reinterpret_cast<int32_t*>(hist), L, out, m, ctl);
       return;
     }
     // too few (lambda above the k-th key) or too many candidates: exact tier
@@ -2269,6 +2231,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
   exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl);
 }
+
 
 // One cluster of G CTAs per row (with kSingle: one CTA, G = 1 at compile time).
 template <int F>

@@ -11,6 +11,7 @@ namespace topk_gb300 {
 enum Form : int { kRaw = 0, kPaged = 1, kRagged = 2, kWindow = 3 };
 
 constexpr int kMaxBins = 4096;         // widest histogram (12 key bits)
+constexpr int kMaxK = 2048;            // largest k (TOPK_MAX_K of the public header)
 constexpr int kTieCapMax = 4096;       // shared tie buffer entries, 8 bytes each
 constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
 
@@ -32,6 +33,7 @@ struct Params {
   int32_t batch;
   int32_t use_filter;          // 1: try the sampled-threshold filter pass first
 };
+
 
 // Problems of one form sharing a launch (kMaxGroup at most; row_begin holds the
 // prefix sums of their batches, row_begin[n] = all rows). Passed by value as a
