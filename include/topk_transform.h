@@ -97,10 +97,22 @@ typedef enum {
  * [1, TOPK_MAX_K] is accepted. */
 #define TOPK_MAX_K 2048
 
-/* Device workspace (bytes) a call with these sizes needs. The kernels keep all
- * per-row state in shared memory, so this is 0 for every size; the workspace
- * arguments below exist so that a future global-memory path does not change the
- * ABI. */
+/* Device workspace (bytes) that lets a single-form call of these sizes on the
+ * current device take the chip-wide split: small batches of long rows (by default
+ * 4 rows up to one row per 16 SMs, rows of at least 65536 elements; see
+ * topk_set_chip_split) are each split over many CTAs anywhere on the chip, which
+ * store their candidates in the workspace for a second kernel that selects per
+ * row. This restates the row split of the exact kernel on the PR #37591 page
+ * ("关键源码片段", row_split and the per-split histograms merged in global memory)
+ * with one sampled threshold instead of merged histograms. 0 when the split does
+ * not apply (then every per-row state stays in shared memory). The size depends on
+ * the SM count and the tie capacity (topk_set_tie_capacity) at the time of the
+ * query. A call given a workspace of at least this size (device memory, 256-byte
+ * aligned, owned by the caller; not read before the call writes it, so it needs no
+ * initialisation; calls that may overlap in time need separate workspaces) takes
+ * the split; a call given less (or NULL) runs the same rows on one cluster of CTAs
+ * per row. The result is the same either way. Returns 0 when no CUDA device is
+ * usable. */
 size_t topk_workspace_bytes(int32_t batch, int64_t max_row_len, int32_t k);
 
 /* Raw form. scores [batch, row_stride] fp32 (row_stride >= 1 elements),
@@ -283,6 +295,11 @@ int topk_reset_guard_hits(void);
  * SM); 0 never (the streaming fast tier). Other values mean 1. The result is the
  * same either way.
  *
+ * topk_set_chip_split(mode): when single-form calls with enough workspace take the
+ * chip-wide split (topk_workspace_bytes): 1 (default) automatically; 2 for every
+ * batch and row length (used by tests); 0 never. Other values mean 1. The result is
+ * the same either way.
+ *
  * topk_set_cta_threads(t): which build of the kernels runs: 512-thread CTAs (two
  * per SM) or 256-thread CTAs (four per SM, at most 3072 tie-buffer entries); any
  * other value restores the built-in choice, which takes the 256-thread build for
@@ -296,6 +313,7 @@ int topk_set_tie_capacity(int cap);
 int topk_set_fast_tier(int enable);
 int topk_set_cta_threads(int threads);
 int topk_set_staged_tier(int mode);
+int topk_set_chip_split(int mode);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -29,7 +29,7 @@ __all__ = [
     "topk_transform_grouped", "TopkProblem", "TOPK_MAX_GROUP", "TOPK_FLAG_SORTED",
     "topk_set_cta_threads", "topk_guard_hits", "topk_reset_guard_hits",
     "topk_workspace_bytes", "topk_set_row_split", "topk_set_tie_capacity", "topk_set_fast_tier",
-    "topk_set_staged_tier",
+    "topk_set_staged_tier", "topk_set_chip_split",
 ]
 
 TOPK_MAX_K = 2048
@@ -101,6 +101,8 @@ def load_library() -> ctypes.CDLL:
             lib.topk_set_fast_tier.argtypes = [ctypes.c_int]
             lib.topk_set_staged_tier.restype = ctypes.c_int
             lib.topk_set_staged_tier.argtypes = [ctypes.c_int]
+            lib.topk_set_chip_split.restype = ctypes.c_int
+            lib.topk_set_chip_split.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -145,6 +147,24 @@ def _stream(stream, device) -> int:
     return int(s.cuda_stream)
 
 
+def _workspace(lib, workspace, batch: int, max_row_len: int, k: int, device, stream):
+    """(pointer, bytes) of the call's workspace: the caller's uint8 tensor, else one
+    allocated here when topk_workspace_bytes asks for one (the chip-wide split)."""
+    if workspace is not None:
+        _cuda_tensor(workspace, "workspace", torch.uint8, device)
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor")
+        return workspace.data_ptr(), int(workspace.numel()), workspace
+    with torch.cuda.device(device):
+        nbytes = int(lib.topk_workspace_bytes(batch, max_row_len, k))
+    if nbytes == 0:
+        return None, 0, None
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)  # in use on that stream until the call's kernels end
+    return ws.data_ptr(), nbytes, ws
+
+
 def _scores_2d(scores: torch.Tensor):
     _cuda_tensor(scores, "scores", torch.float32)
     if scores.dim() != 2 or not scores.is_contiguous() or scores.shape[1] < 1:
@@ -157,23 +177,26 @@ def topk_workspace_bytes(batch: int, max_row_len: int, k: int) -> int:
 
 
 def topk_transform_raw(scores: torch.Tensor, seq_lens: torch.Tensor, k: int,
-                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Exact top-k positions of each row of ``scores`` (raw form)."""
+                       out: torch.Tensor | None = None, stream=None,
+                       workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact top-k positions of each row of ``scores`` (raw form). workspace: a uint8
+    device tensor of topk_workspace_bytes (else allocated here when needed)."""
     lib = load_library()
     batch, row_stride = _scores_2d(scores)
     dev = scores.device
     _vector(seq_lens, "seq_lens", batch, dev)
     out = _out(out, batch, k, dev)
+    ws, ws_bytes, _keep = _workspace(lib, workspace, batch, row_stride, k, dev, stream)
     with torch.cuda.device(dev):
         st = lib.topk_transform_raw(scores.data_ptr(), row_stride, seq_lens.data_ptr(), batch, k,
-                                    out.data_ptr(), None, 0, _stream(stream, dev))
+                                    out.data_ptr(), ws, ws_bytes, _stream(stream, dev))
     _check(st, "topk_transform_raw")
     return out
 
 
 def topk_transform_paged(scores: torch.Tensor, seq_lens: torch.Tensor, page_table: torch.Tensor,
                          page_size: int, k: int, out: torch.Tensor | None = None,
-                         stream=None) -> torch.Tensor:
+                         stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Exact top-k of each row, each position j written as
     page_table[b, j // page_size] * page_size + j % page_size."""
     lib = load_library()
@@ -190,17 +213,18 @@ def topk_transform_paged(scores: torch.Tensor, seq_lens: torch.Tensor, page_tabl
     if page_table.shape[1] * page_size < min(row_stride, scores.shape[1]):
         raise ValueError("page_table has too few pages for the rows")
     out = _out(out, batch, k, dev)
+    ws, ws_bytes, _keep = _workspace(lib, workspace, batch, row_stride, k, dev, stream)
     with torch.cuda.device(dev):
         st = lib.topk_transform_paged(scores.data_ptr(), row_stride, seq_lens.data_ptr(),
                                       page_table.data_ptr(), pt_stride, page_size, batch, k,
-                                      out.data_ptr(), None, 0, _stream(stream, dev))
+                                      out.data_ptr(), ws, ws_bytes, _stream(stream, dev))
     _check(st, "topk_transform_paged")
     return out
 
 
 def topk_transform_ragged(scores: torch.Tensor, row_starts: torch.Tensor, seq_lens: torch.Tensor,
                           k: int, max_row_len_hint: int = 0, out: torch.Tensor | None = None,
-                          stream=None) -> torch.Tensor:
+                          stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Exact top-k of packed rows scores[row_starts[b] : row_starts[b] + seq_lens[b]];
     each position j is written as row_starts[b] + j."""
     lib = load_library()
@@ -212,17 +236,18 @@ def topk_transform_ragged(scores: torch.Tensor, row_starts: torch.Tensor, seq_le
     _vector(row_starts, "row_starts", batch, dev)
     _vector(seq_lens, "seq_lens", batch, dev)
     out = _out(out, batch, k, dev)
+    ws, ws_bytes, _keep = _workspace(lib, workspace, batch, int(max_row_len_hint), k, dev, stream)
     with torch.cuda.device(dev):
         st = lib.topk_transform_ragged(scores.data_ptr(), row_starts.data_ptr(),
                                        seq_lens.data_ptr(), int(max_row_len_hint), batch, k,
-                                       out.data_ptr(), None, 0, _stream(stream, dev))
+                                       out.data_ptr(), ws, ws_bytes, _stream(stream, dev))
     _check(st, "topk_transform_ragged")
     return out
 
 
 def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: torch.Tensor,
                           k: int, max_row_len_hint: int = 0, out: torch.Tensor | None = None,
-                          stream=None) -> torch.Tensor:
+                          stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Exact top-k of each row's window of columns [starts[b], seq_lens[b]) (both
     clamped to the row); the selected columns are written. max_row_len_hint: an
     upper bound of the window lengths (0: the row length), used only to pick the
@@ -233,10 +258,12 @@ def topk_transform_window(scores: torch.Tensor, starts: torch.Tensor, seq_lens: 
     _vector(starts, "starts", batch, dev)
     _vector(seq_lens, "seq_lens", batch, dev)
     out = _out(out, batch, k, dev)
+    hint = int(max_row_len_hint) if 0 < int(max_row_len_hint) < row_stride else row_stride
+    ws, ws_bytes, _keep = _workspace(lib, workspace, batch, hint, k, dev, stream)
     with torch.cuda.device(dev):
         st = lib.topk_transform_window(scores.data_ptr(), row_stride, starts.data_ptr(),
                                        seq_lens.data_ptr(), int(max_row_len_hint), batch, k,
-                                       out.data_ptr(), None, 0, _stream(stream, dev))
+                                       out.data_ptr(), ws, ws_bytes, _stream(stream, dev))
     _check(st, "topk_transform_window")
     return out
 
@@ -391,6 +418,13 @@ def topk_set_cta_threads(threads: int) -> int:
 def topk_set_fast_tier(enable: bool) -> int:
     """1: try the sampled-threshold one-pass filter first (default); 0: exact tier only."""
     return int(load_library().topk_set_fast_tier(1 if enable else 0))
+
+
+def topk_set_chip_split(mode: int) -> int:
+    """When single-form calls take the chip-wide split (many CTAs per row, candidates
+    through a device workspace): 1 automatic (default), 2 for every batch and row
+    length, 0 never."""
+    return int(load_library().topk_set_chip_split(int(mode)))
 
 
 def topk_set_staged_tier(mode: int) -> int:

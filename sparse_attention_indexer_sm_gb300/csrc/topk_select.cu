@@ -666,16 +666,21 @@ __device__ __forceinline__ void emit_pad(int32_t* out, uint32_t slot, const OutM
 // quads and the row position of each quad's first element (INT32_MAX when the
 // thread has no quad). An element counts only if its position is below the row's
 // length, which for the raw and paged forms is read while the sample is in flight.
-struct Sample {
-  uint32_t key[4 * kSampleQuads];
-  int32_t j[kSampleQuads];
+template <int Q = kSampleQuads>
+struct SampleT {
+  static constexpr int kQuads = Q;  // sampled quads per thread
+  uint32_t key[4 * Q];
+  int32_t j[Q];
 };
+using Sample = SampleT<>;
 
 // The sample is taken in runs of 32 consecutive quads (512 bytes, one per warp and
 // round) spread evenly over the slice: whole DRAM bursts instead of one 16-byte
 // piece of every few lines, so the sample arrives sooner; the later stream finds
 // these lines in L2.
-__device__ __forceinline__ void load_sample(const Slice& s, Sample& sm) {
+template <class Smp>
+__device__ __forceinline__ void load_sample(const Slice& s, Smp& sm) {
+  constexpr int kSampleQuads = Smp::kQuads;
   constexpr int32_t kRuns = kWarps * kSampleQuads;
   const int32_t spacing = max(32, s.nq / kRuns);  // quads from one run to the next
 #pragma unroll
@@ -692,7 +697,8 @@ __device__ __forceinline__ void load_sample(const Slice& s, Sample& sm) {
   }
 }
 
-__device__ __forceinline__ bool sample_valid(const Sample& sm, int i, int32_t L) {
+template <class Smp>
+__device__ __forceinline__ bool sample_valid(const Smp& sm, int i, int32_t L) {
   return sm.j[i / 4] < L - (i & 3);
 }
 
@@ -711,10 +717,12 @@ __device__ __forceinline__ void merge_into_cta0(const uint32_t* h, uint32_t* mh,
 // the header comment). The kH1 and kH2 regions of `hist` and of CTA 0's `mhist`
 // are zero on entry, and so is CTA 0's ctl.ns. Returns lambda; *shift2 gets the
 // candidate-histogram bin width exponent.
-__device__ __forceinline__ uint32_t sample_lambda(const Sample& sm, const Slice& s, bool prefetched,
+template <class Smp>
+__device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s, bool prefetched,
                                                   int32_t L, uint32_t k, int G, int rank,
                                                   uint32_t* hist, uint32_t* mhist, Ctl& ctl,
                                                   uint32_t* shift2) {
+  constexpr int kSampleQuads = Smp::kQuads;
   const int tid = threadIdx.x;
   const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
   // round 1: coarse bins (top 10 key bits), one shared atomic per sample key (this
@@ -2232,6 +2240,245 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl);
 }
 
+// ------------------------------------------------------------------ chip-wide split
+//
+// Small batches of long rows: each row is split over split_s CTAs anywhere on the
+// chip (not one cluster), in two kernels. The filter kernel's CTAs each take the
+// same sampled threshold of the whole row and store their slice's candidates in the
+// workspace; the select kernel (one CTA per row, after the filter kernel) gathers
+// them and selects. A row whose candidates do not fit (a CTA's share over
+// split_cap, or the row's over gather_cap) or fall short of k takes the exact tier
+// on the select CTA.
+
+// The row's data, valid length and output map (page table not staged).
+template <int F>
+__device__ __forceinline__ void row_view(const Params& p, int row, int32_t seq, int32_t start,
+                                         const float** rowp, int32_t* L, OutMap* m) {
+  m->pt_row = nullptr;
+  m->pt_smem = nullptr;
+  m->pt_n = 0;
+  m->ps = p.page_size;
+  m->ps_shift = p.page_shift;
+  m->rstart = 0;
+  m->values = nullptr;
+  m->staged = nullptr;
+  if constexpr (form_of(F) == kRagged) {
+    m->rstart = start;
+    *rowp = p.scores + start;
+    *L = max(seq, 0);
+  } else if constexpr (form_of(F) == kWindow) {
+    const int64_t hi = min(static_cast<int64_t>(max(seq, 0)), p.row_stride);
+    const int64_t lo = min(static_cast<int64_t>(max(start, 0)), hi);
+    m->rstart = static_cast<int32_t>(lo);
+    *rowp = p.scores + static_cast<int64_t>(row) * p.row_stride + lo;
+    *L = static_cast<int32_t>(hi - lo);
+  } else {
+    *rowp = p.scores + static_cast<int64_t>(row) * p.row_stride;
+    *L = static_cast<int32_t>(min(static_cast<int64_t>(max(seq, 0)), p.row_stride));
+  }
+  if constexpr (form_of(F) == kPaged) {
+    m->pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+    const int64_t up = static_cast<int64_t>(*L) + p.page_size - 1;
+    const int64_t np = p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size;
+    m->pt_n = static_cast<int32_t>(min(np, p.pt_stride));
+  }
+}
+
+// Filter CTA `part` (of p.split_s) of row `row`. Shared memory: histogram | buffer of
+// split_cap candidates.
+template <int F>
+__device__ __forceinline__ void split_filter_part(const Params& p, int row, int part, uint32_t* dyn,
+                                                  Ctl& ctl) {
+  const int tid = threadIdx.x;
+  const int S = p.split_s;
+  uint32_t* hist = dyn;
+  uint2* buf = reinterpret_cast<uint2*>(dyn + kHistWords);
+  const uint32_t cap = static_cast<uint32_t>(p.split_cap);
+  allow_next_grid();
+  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (tid == 0) {
+    ctl.cand_cnt = 0;
+    ctl.ns = 0;
+    ctl.lambda = 0;
+    ctl.lambda_shift = 0;
+  }
+  wait_prior_grids();  // the workspace is free once the previous launch has ended
+  const int32_t seq = p.seq_lens[row];
+  int32_t start = 0;
+  if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) start = p.row_starts[row];
+  // raw, paged: the sample of the whole stride while the length is on its way
+  // a sample four times the streaming tier's (8192 keys): the threshold lies
+  // closer to the k-th key, so the select CTA gathers fewer candidates
+  SampleT<4 * kSampleQuads> sm;
+  bool sample_loaded = false;
+  if constexpr (form_of(F) == kRaw || form_of(F) == kPaged) {
+    if (p.row_stride > static_cast<int64_t>(p.gather_cap) && p.row_stride <= INT32_MAX) {
+      load_sample(make_slice(p.scores + static_cast<int64_t>(row) * p.row_stride,
+                             static_cast<int32_t>(p.row_stride), 0, 1),
+                  sm);
+      sample_loaded = true;
+    }
+  }
+  const float* rowp;
+  int32_t L;
+  OutMap m;
+  row_view<F>(p, row, seq, start, &rowp, &L, &m);
+  const int32_t k = p.k;
+  uint2* hdr = reinterpret_cast<uint2*>(p.split_ws);
+  int32_t* counts =
+      reinterpret_cast<int32_t*>(static_cast<char*>(p.split_ws) + split_counts_offset(p.batch));
+  uint2* entries =
+      reinterpret_cast<uint2*>(static_cast<char*>(p.split_ws) + split_entries_offset(p.batch, S));
+  const int64_t cell = static_cast<int64_t>(row) * S + part;
+  if (L <= k) {  // the select CTA writes such rows alone
+    if (tid == 0) counts[cell] = 0;
+    return;
+  }
+  const Slice s = make_slice(rowp, L, part, S);
+  // rows that fit the select CTA's buffer skip the sample: every element is a candidate
+  const bool sampled = static_cast<uint32_t>(L) > static_cast<uint32_t>(p.gather_cap);
+  if (sampled && !sample_loaded) load_sample(make_slice(rowp, L, 0, 1), sm);
+  prefetch_slice(s, kThreads - 32);
+  __syncthreads();  // the cleared histogram and counters
+  uint32_t shift2 = 32 - kCandBits;
+  const uint32_t lambda =
+      sampled ? sample_lambda(sm, s, true, L, static_cast<uint32_t>(k), 1, 0, hist, nullptr, ctl, &shift2)
+              : 0u;
+  if (lambda >= 0x80000000u)
+    filter_positions<true, true>(s, lambda, shift2, buf, cap, hist + kHC, ctl);
+  else
+    filter_positions<false, true>(s, lambda, shift2, buf, cap, hist + kHC, ctl);
+  __syncthreads();
+  const uint32_t n = ctl.cand_cnt;
+  const uint32_t stored = min(n, cap);
+  uint2* dst = entries + cell * cap;
+  for (uint32_t i = static_cast<uint32_t>(tid); i < stored; i += kThreads) dst[i] = buf[i];
+  if (tid == 0) {
+    counts[cell] = static_cast<int32_t>(min(n, static_cast<uint32_t>(INT32_MAX)));
+    if (part == 0) hdr[row] = make_uint2(lambda, shift2);
+  }
+}
+
+// The select CTA of row `row`: gathers the filter CTAs' candidates (and their
+// histogram) and selects; shared memory as row_body's for one CTA, with a buffer of
+// gather_cap candidates.
+template <int F>
+__device__ __forceinline__ void split_select_row(const Params& p, int row, uint32_t* dyn, Ctl& ctl) {
+  const int tid = threadIdx.x;
+  const int S = p.split_s;
+  uint32_t* hist = dyn;
+  uint2* list = reinterpret_cast<uint2*>(dyn + kHistWords);
+  int32_t* pt_smem = reinterpret_cast<int32_t*>(dyn + kHistWords + kListWords);
+  uint2* buf = reinterpret_cast<uint2*>(dyn + kHistWords + kListWords + kPtCap);
+  const uint32_t gcap = static_cast<uint32_t>(p.gather_cap);
+  allow_next_grid();
+  for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (tid == 0) {
+    ctl.win_cnt = 0;
+    ctl.tie_cnt = 0;
+    ctl.out_cnt = 0;
+    ctl.cand_cnt = 0;
+  }
+  wait_prior_grids();  // the filter kernel's candidates (and whatever the inputs wait for)
+  // the parts' counts and the row's threshold, read together with the row's length
+  // (meaningless for rows of at most k elements, which do not use them)
+  const uint2* hdr = reinterpret_cast<const uint2*>(p.split_ws);
+  const int32_t* counts = reinterpret_cast<const int32_t*>(static_cast<const char*>(p.split_ws) +
+                                                           split_counts_offset(p.batch));
+  const int32_t c = tid < S ? counts[static_cast<int64_t>(row) * S + tid] : 0;
+  const uint2 lh = hdr[row];
+  const int32_t seq = p.seq_lens[row];
+  int32_t start = 0;
+  if constexpr (form_of(F) == kRagged || form_of(F) == kWindow) start = p.row_starts[row];
+  const float* rowp;
+  int32_t L;
+  OutMap m;
+  row_view<F>(p, row, seq, start, &rowp, &L, &m);
+  const int32_t k = p.k;
+  int32_t* out = p.out + static_cast<int64_t>(row) * k;
+  if constexpr (form_of(F) == kPaged) {
+    const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
+    if ((p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size) > p.pt_stride && tid == 0)
+      guard_hit();
+  }
+  int32_t pages = 0;
+  if constexpr (form_of(F) == kPaged) {
+    if (m.pt_n <= kPtCap) {
+      pages = m.pt_n;
+      for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, m.pt_row + i);
+    }
+  }
+  if (L <= k) {
+    cp_async_wait_all();
+    __syncthreads();
+    if (pages > 0) m.pt_smem = pt_smem;
+    for (int32_t i = tid; i < k; i += kThreads) {
+      if (i < L)
+        emit<F>(out, k, static_cast<uint32_t>(i), m, i, 0u);
+      else
+        emit_pad<F>(out, static_cast<uint32_t>(i), m);
+    }
+    return;
+  }
+  const uint2* entries = reinterpret_cast<const uint2*>(static_cast<const char*>(p.split_ws) +
+                                                        split_entries_offset(p.batch, S));
+  const uint32_t scap = static_cast<uint32_t>(p.split_cap);
+  // the parts' counts: an exclusive scan over the first S threads (S <= kThreads)
+  uint32_t total = 0;
+  const uint32_t off = block_excl_scan(static_cast<uint32_t>(c), ctl, &total);
+  const bool over = __syncthreads_or(static_cast<uint32_t>(c) > scap) != 0;
+  int32_t* part_off = reinterpret_cast<int32_t*>(list);  // S + 1 offsets, then the scan is read
+  if (tid < S) part_off[tid] = static_cast<int32_t>(off);
+  if (tid == 0) part_off[S] = static_cast<int32_t>(total);
+  cp_async_wait_all();
+  __syncthreads();
+  if (pages > 0) m.pt_smem = pt_smem;
+  if (__builtin_expect(over || total < static_cast<uint32_t>(k) || total > gcap, 0)) {
+    // exact tier over the whole row on this CTA
+    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    exact_tier<F>(make_slice(rowp, L, 0, 1), L, k, out, m, pages, pt_smem, 1, 0, hist, nullptr, buf,
+                  min(gcap, static_cast<uint32_t>(kTieCapMax)), ctl);
+    return;
+  }
+  const uint32_t lambda = lh.x, shift = lh.y;
+  uint32_t* chist = hist + kHC;
+  // gather: kThreads / S threads per part, each taking every (kThreads / S)-th entry
+  // of it, eight loads in flight at a time
+  uint32_t top = 0;
+  {
+    const int tpp = kThreads / S;  // S is a power of two <= kMaxSplit <= kThreads
+    const int part = tid / tpp, sub = tid % tpp;
+    const uint32_t cnt = static_cast<uint32_t>(part_off[part + 1] - part_off[part]);
+    const uint2* src = entries + (static_cast<int64_t>(row) * S + part) * scap;
+    uint2* dst = buf + part_off[part];
+    for (uint32_t b = static_cast<uint32_t>(sub); b < cnt; b += 8u * static_cast<uint32_t>(tpp)) {
+      uint2 e[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = b + static_cast<uint32_t>(u * tpp);
+        e[u] = i < cnt ? src[i] : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t i = b + static_cast<uint32_t>(u * tpp);
+        if (i < cnt) {
+          dst[i] = e[u];
+          const uint32_t d = (e[u].x - lambda) >> shift;
+          if (d >= static_cast<uint32_t>(kCandBins - 1))
+            ++top;
+          else
+            atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+        }
+      }
+    }
+  }
+  top = __reduce_add_sync(kFull, top);
+  if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
+  __syncthreads();  // buffer, histogram; the offsets in list are read no more
+  select_candidates<F>(buf, total, static_cast<uint32_t>(k), chist, lambda, shift, list, hist,
+                       reinterpret_cast<int32_t*>(hist), L, out, m, ctl);
+}
 
 // One cluster of G CTAs per row (with kSingle: one CTA, G = 1 at compile time).
 template <int F>
@@ -2268,6 +2515,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     staged_row<F>(prob, item - gp.row_begin[i], dyn, ctl);
   else
     row_body<F>(prob, item - gp.row_begin[i], G, static_cast<int>(cluster_ctarank()), dyn, ctl);
+}
+
+// The chip-wide split's two kernels (split_filter_part, split_select_row).
+template <int F>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_split_filter_kernel(const Params p) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  __shared__ Ctl ctl;
+  const int S = p.split_s;
+  split_filter_part<F>(p, static_cast<int>(blockIdx.x) / S, static_cast<int>(blockIdx.x) % S, dyn, ctl);
+}
+template <int F>
+__global__ void __launch_bounds__(kThreads) topk_split_select_kernel(const Params p) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  __shared__ Ctl ctl;
+  split_select_row<F>(p, static_cast<int>(blockIdx.x), dyn, ctl);
 }
 
 // The sort pass of the sorted output (one CTA per row, after the selection kernel):
@@ -2345,6 +2607,10 @@ __global__ void __launch_bounds__(kThreads) topk_sort_kernel(const Params p) {
 constexpr size_t rows_smem_bytes(int g, int tie_cap) {
   return sizeof(uint32_t) * static_cast<size_t>(kHistWords * (g > 1 ? 2 : 1) + kListWords + kPtCap) +
          sizeof(uint2) * static_cast<size_t>(tie_cap);
+}
+// The chip-wide split's filter CTA: histogram | its candidate buffer.
+constexpr size_t split_filter_smem_bytes(int split_cap) {
+  return sizeof(uint32_t) * static_cast<size_t>(kHistWords) + sizeof(uint2) * static_cast<size_t>(split_cap);
 }
 template <bool kHalf>
 constexpr size_t staged_smem_bytes(int tie_cap) {
@@ -2432,6 +2698,10 @@ cudaError_t prepare_device() {
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts | kKeysInFilter>);
   if (e == cudaSuccess) e = prepare_kernel(topk_group_kernel<F | kOpts>);
+  if (e == cudaSuccess)
+    e = prepare_kernel(topk_split_filter_kernel<F>, split_filter_smem_bytes(kSplitCapMax));
+  if (e == cudaSuccess)
+    e = prepare_kernel(topk_split_select_kernel<F>, rows_smem_bytes(1, kGatherCapMax));
   if constexpr (kHasStaged) {
     const size_t full = staged_smem_bytes<false>(kTieCapMax), half = staged_smem_bytes<true>(kTieCapMax);
     if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kStaged>, full);
@@ -2476,6 +2746,30 @@ cudaError_t launch_group(const GroupParams& gp, int g, bool opts, bool keys_in_f
                 : launch_group_form<F | kOpts>(gp, g, stream);
   return keys ? launch_group_form<F | kKeysInFilter>(gp, g, stream)
               : launch_group_form<F>(gp, g, stream);
+}
+
+cudaError_t launch_split(const Params& p, cudaStream_t stream) {
+  constexpr int F = kForm;
+  if (p.split_s < 1 || p.split_s > kMaxSplit || (p.split_s & (p.split_s - 1)) != 0 ||
+      p.split_cap < 0 || p.split_cap > kSplitCapMax || p.gather_cap < 0 ||
+      p.gather_cap > kGatherCapMax || p.split_ws == nullptr || p.values != nullptr ||
+      p.staged != nullptr)
+    return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(p.batch) * p.split_s), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = split_filter_smem_bytes(p.split_cap);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_split_filter_kernel<F>, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
+  cfg.dynamicSmemBytes = rows_smem_bytes(1, p.gather_cap);
+  return cudaLaunchKernelEx(&cfg, topk_split_select_kernel<F>, p);
 }
 
 cudaError_t sort_rows(const Params& p, cudaStream_t stream) {
@@ -2540,6 +2834,16 @@ cudaError_t launch_group(Form form, const GroupParams& gp, int g, bool opts,
     case kPaged: return paged::launch_group(gp, g, opts, keys_in_filter, staged, stream);
     case kRagged: return ragged::launch_group(gp, g, opts, keys_in_filter, staged, stream);
     case kWindow: return window::launch_group(gp, g, opts, keys_in_filter, staged, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_split(Form form, const Params& p, cudaStream_t stream) {
+  switch (form) {
+    case kRaw: return raw::launch_split(p, stream);
+    case kPaged: return paged::launch_split(p, stream);
+    case kRagged: return ragged::launch_split(p, stream);
+    case kWindow: return window::launch_split(p, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -32,8 +32,30 @@ struct Params {
   int32_t tie_cap;             // <= kTieCapMax
   int32_t batch;
   int32_t use_filter;          // 1: try the sampled-threshold filter pass first
+  // chip-wide split (split_s > 0): split_s CTAs per row filter their slices into the
+  // workspace split_ws (split_workspace_bytes), a second kernel selects per row
+  void* split_ws;
+  int32_t split_s;             // CTAs per row: a power of two, at most kMaxSplit
+  int32_t split_cap;           // candidates one filter CTA may store
+  int32_t gather_cap;          // candidates the select CTA may gather
 };
 
+// The chip-wide split's workspace for `rows` rows of `s` CTAs storing up to `cap`
+// candidates each: per row the threshold and bin width (uint2), per CTA its
+// candidate count (int32), per CTA `cap` (key, position) pairs; each part 256-byte
+// aligned.
+constexpr int kMaxSplit = 256;
+constexpr int kSplitCapMax = 256;     // candidates one filter CTA may store, at most
+constexpr int kGatherCapMax = 16384;  // candidates the select CTA may gather, at most
+__host__ __device__ constexpr size_t split_align(size_t b) { return (b + 255u) / 256u * 256u; }
+__host__ __device__ constexpr size_t split_counts_offset(int64_t rows) { return split_align(8u * static_cast<size_t>(rows)); }
+__host__ __device__ constexpr size_t split_entries_offset(int64_t rows, int s) {
+  return split_counts_offset(rows) + split_align(4u * static_cast<size_t>(rows) * static_cast<size_t>(s));
+}
+__host__ __device__ constexpr size_t split_workspace_bytes(int64_t rows, int s, int cap) {
+  return split_entries_offset(rows, s) +
+         split_align(8u * static_cast<size_t>(rows) * static_cast<size_t>(s) * static_cast<size_t>(cap));
+}
 
 // Problems of one form sharing a launch (kMaxGroup at most; row_begin holds the
 // prefix sums of their batches, row_begin[n] = all rows). Passed by value as a
@@ -73,6 +95,9 @@ constexpr int kTieCap256 = 3072;
   /* The sort pass of the sorted output: p.staged (filled by a launch with p) is */     \
   /* ordered per row and written to p.out and p.values; one CTA per row. */             \
   cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream);                \
+  /* Enqueue the chip-wide split (p.split_*: set; no values or sorted output): */        \
+  /* batch * split_s filter CTAs, then one select CTA per row. */                       \
+  cudaError_t launch_split(Form form, const Params& p, cudaStream_t stream);             \
   /* The count of failed internal consistency checks on the current device (a */       \
   /* synchronous read), and its reset. */                                               \
   cudaError_t guard_hits(unsigned int* hits);                                           \
@@ -87,6 +112,7 @@ constexpr int kTieCap256 = 3072;
   cudaError_t launch_group(const GroupParams& gp, int g, bool opts, bool keys_in_filter, \
                            int staged, cudaStream_t stream);                            \
   cudaError_t sort_rows(const Params& p, cudaStream_t stream);                          \
+  cudaError_t launch_split(const Params& p, cudaStream_t stream);                       \
   cudaError_t guard_hits(unsigned int* hits);                                           \
   cudaError_t reset_guard_hits();
 

@@ -64,7 +64,8 @@ def test_host_side_argument_checks(lib):
     assert lib.topk_transform_paged(one, 8, one, one, 0, 64, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_ragged(one, None, one, 0, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_ragged(one, one, one, -1, 1, 16, one, None, 0, None) == 1
-    assert lib.topk_workspace_bytes(256, 262144, 2048) == 0
+    assert lib.topk_workspace_bytes(256, 262144, 2048) == 0  # no device here: no split
+    assert lib.topk_workspace_bytes(1, 262144, 2048) == 0
     assert lib.topk_transform_window(one, 8, None, one, 0, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_window(one, 0, one, one, 0, 1, 16, one, None, 0, None) == 1
     assert lib.topk_transform_window(one, 8, one, one, -1, 1, 16, one, None, 0, None) == 1

@@ -39,7 +39,10 @@ def no_guard_hits(pkg):
 
 
 @contextlib.contextmanager
-def settings(pkg, split=None, tie_cap=None, fast=None, cta=None, staged=None):
+def settings(pkg, split=None, tie_cap=None, fast=None, cta=None, staged=None, chip=None):
+    if split is not None and chip is None:
+        chip = 0  # a forced cluster split is what such a test exercises
+    prev_chip = pkg.topk_set_chip_split(chip) if chip is not None else None
     prev_split = pkg.topk_set_row_split(split) if split is not None else None
     prev_cap = pkg.topk_set_tie_capacity(tie_cap) if tie_cap is not None else None
     prev_fast = pkg.topk_set_fast_tier(fast) if fast is not None else None
@@ -48,6 +51,8 @@ def settings(pkg, split=None, tie_cap=None, fast=None, cta=None, staged=None):
     try:
         yield
     finally:
+        if chip is not None:
+            pkg.topk_set_chip_split(prev_chip)
         if staged is not None:
             pkg.topk_set_staged_tier(prev_staged)
         if cta is not None:
@@ -133,8 +138,84 @@ def test_config4_adversarial_ragged(pkg, dist):
 
 @pytest.mark.parametrize("batch", [1, 2, 4])
 def test_config5_long_rows(pkg, batch):
+    """Small batches of 262144-element rows: the chip-wide split from 4 rows on
+    (automatic), clusters below."""
+    assert (pkg.topk_workspace_bytes(batch, 262144, 2048) > 0) == (batch >= 4)
     w = workloads.config5(batch)
     assert_parity(w, run_gpu(pkg, w), check_rows=2)
+
+
+@pytest.mark.parametrize("batch,chip", [(1, 2), (4, 0)])
+def test_config5_long_rows_other_path(pkg, batch, chip):
+    """The same rows on the path the automatic rule does not pick: the chip-wide split
+    for one row, clusters for four."""
+    w = workloads.config5(batch)
+    with settings(pkg, chip=chip):
+        assert (pkg.topk_workspace_bytes(batch, 262144, 2048) > 0) == (chip == 2)
+        got = run_gpu(pkg, w)
+    assert_parity(w, got, check_rows=2)
+
+
+# ------------------------------------------------------------ the chip-wide split
+
+@pytest.mark.parametrize("tie_cap", [None, 0, 16, 300])
+@pytest.mark.parametrize("dist", ["normal", "decode", "banded", "narrow", "subnormal", "heavy_tail"])
+def test_chip_split_forced(pkg, dist, tie_cap):
+    """The chip-wide split forced onto paged rows of random lengths (some shorter than
+    k); small tie capacities shrink its candidate stores, so rows take its fallback."""
+    w = _mixed(900, dist)
+    with settings(pkg, chip=2, tie_cap=tie_cap):
+        assert pkg.topk_workspace_bytes(w.batch, w.scores.shape[1], w.k) > 0
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+@pytest.mark.parametrize("k", [1, 7, 1024, 2048])
+@pytest.mark.parametrize("form", ["raw", "ragged", "window"])
+def test_chip_split_forms(pkg, form, k):
+    """Every form through the chip-wide split: odd row offsets, empty rows, rows
+    shorter than k, duplicates."""
+    g = workloads.rng(910 + k)
+    if form == "ragged":
+        lens = np.array([0, 1, 2047, 2048, 2049, 70001, 3, 150000, 0, 65536], np.int64)
+        gaps = g.integers(0, 7, size=lens.shape[0])
+        starts = (np.concatenate([[0], np.cumsum(lens + gaps)[:-1]]) + 1).astype(np.int32)
+        total = int(starts[-1] + lens[-1] + 5)
+        scores = workloads.row_values(g, "banded", total, dup=True)
+        w = workloads.Workload(f"chip_ragged_k{k}", "ragged", k, scores, lens.astype(np.int32),
+                               None, 64, starts)
+    elif form == "window":
+        batch, stride = 5, 70001
+        scores = workloads.random_rows(g, batch, stride, "decode", dup=True)
+        hi = g.integers(0, stride + 3, size=batch).astype(np.int32)
+        lo = (hi * g.random(batch) * 0.5).astype(np.int32)
+        w = workloads.Workload(f"chip_window_k{k}", "window", k, scores, hi, None, 64, lo)
+    else:
+        w = _mixed(920 + k, "heavy_tail", batch=5, stride=70001, k=k).as_raw()
+    with settings(pkg, chip=2):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
+def test_chip_split_workspace(pkg):
+    """A caller's workspace, reused without initialisation, gives the same rows; one
+    too small sends the call to the cluster path, with the same result."""
+    w = workloads.config5(4)
+    dev = torch.device("cuda:0")
+    scores = torch.from_numpy(w.scores).to(dev)
+    seq = torch.from_numpy(w.seq_lens).to(dev)
+    pt = torch.from_numpy(w.page_table).to(dev)
+    need = pkg.topk_workspace_bytes(w.batch, w.scores.shape[1], w.k)
+    assert need > 0
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device=dev)  # garbage contents
+    outs = []
+    for wsx in (ws, ws, ws[: need - 256]):
+        out = torch.full((w.batch, w.k), -7, dtype=torch.int32, device=dev)
+        pkg.topk_transform_paged(scores, seq, pt, w.page_size, w.k, out=out, workspace=wsx)
+        outs.append(out.cpu().numpy())
+    torch.cuda.synchronize()
+    for got in outs:
+        assert_parity(w, got, check_rows=1)
 
 
 # ------------------------------------------------------------ a page table narrower than a row
