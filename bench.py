@@ -62,7 +62,54 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--repeats", type=int, default=11,
                     help="timed windows of exactly --steps calls; the median is reported")
+    ap.add_argument("--profile-workload", default=None, metavar="NAME",
+                    help="only run --warmup then --steps plain calls of one workload (for ncu "
+                         "captures; nothing is timed): " + ", ".join(PROFILE_WORKLOADS))
     return ap.parse_args()
+
+
+PROFILE_WORKLOADS = ("c1", "c2-8192", "c2-32768", "c3-b<B>-paged", "c3-b<B>-raw", "c4-banded",
+                     "c4-narrow", "c4-subnormal", "c5-b<B>", "window-causal", "window-w8192")
+
+
+def named_workload(name: str):
+    """The workload a --profile-workload name stands for (the sweep's configurations)."""
+    if name == "c1":
+        return workloads.config1()
+    if name.startswith("c2-"):
+        return workloads.config2(int(name[3:]))
+    if name.startswith("c3-b"):
+        b, form = name[4:].split("-")
+        return workloads.config3(int(b), form)
+    if name.startswith("c4-"):
+        return workloads.config4(name[3:])
+    if name.startswith("c5-b"):
+        return workloads.config5(int(name[4:]))
+    if name == "window-causal":
+        return workloads.prefill_windows(4096, C4_LEN, window=None)
+    if name == "window-w8192":
+        return workloads.prefill_windows(4096, C4_LEN, window=8192)
+    raise SystemExit(f"unknown workload {name!r}; one of: " + ", ".join(PROFILE_WORKLOADS))
+
+
+def run_profile_workload(args):
+    """--warmup then --steps plain calls of one workload on rotating input sets (inputs
+    beyond L2 as in the timed runs), for a profiler to capture; prints one line."""
+    import torch
+    import sparse_attention_indexer_sm_gb300 as pkg
+    w = named_workload(args.profile_workload)
+    dev = torch.device("cuda:0")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = w.scores.nbytes + w.seq_lens.nbytes + (w.page_table.nbytes if w.form == "paged" else 0)
+    n_sets = max(2, min(64, math.ceil(L2_FACTOR * l2 / set_bytes)))
+    sets = device_sets(w, n_sets, dev, torch)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            call(pkg, w, sets[i % n_sets], stream)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_workload": args.profile_workload, "name": w.name,
+                      "calls": args.warmup + args.steps, "input_sets": n_sets}), flush=True)
 
 
 def algorithmic_bytes(batch: int, L: int, k: int, form: str, page_size: int = PAGE_SIZE) -> int:
@@ -642,7 +689,9 @@ def run_reference(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.profile_workload is not None:
+        run_profile_workload(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
