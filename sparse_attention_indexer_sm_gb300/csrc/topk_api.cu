@@ -40,6 +40,8 @@ struct DeviceState {
   // failed lookup is not remembered: the next call tries again).
   std::mutex stage_mu;
   std::atomic<void*> stage{nullptr};
+  // clusters of 4, 8 and 16 CTAs the device holds at once (0: not known)
+  int clusters4 = 0, clusters8 = 0, clusters16 = 0;
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -61,7 +63,8 @@ int row_split_setting() {
 // 32 blocks, none when fewer than 4). Here a split costs no extra launch (the CTAs
 // of a cluster merge histograms in distributed shared memory); the rule below is
 // the measured one. row_len <= 0 means unknown: treated as long.
-int choose_split(int64_t batch, int64_t row_len, int sm_count) {
+int choose_split(int64_t batch, int64_t row_len, const DeviceState& ds) {
+  const int sm_count = ds.sm_count;
   const int forced = row_split_setting();
   if (forced >= 1) {
     int g = 1;
@@ -79,6 +82,14 @@ int choose_split(int64_t batch, int64_t row_len, int sm_count) {
   int g = 1;
   while (g < topk_gb300::kMaxCluster && len / (g * 2) >= 8192) g *= 2;
   while (g > 1 && batch * g > slots) g /= 2;
+  // and the rows' clusters resident at once: the hardware places a cluster within one
+  // GPC, so fewer clusters of 16 fit than SMs alone allow (C4, 16 rows of 65536-262144
+  // elements: a second wave of clusters at G = 16)
+  auto fits = [&](int gg) {
+    const int n = gg == 16 ? ds.clusters16 : gg == 8 ? ds.clusters8 : gg == 4 ? ds.clusters4 : 0;
+    return n <= 0 || batch <= n;
+  };
+  while (g > 4 && !fits(g)) g /= 2;
   return g >= 4 ? g : 1;
 }
 
@@ -158,6 +169,13 @@ int device_state(DeviceState** out) {
     ds.err = cudaDeviceGetAttribute(&ds.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (ds.err == cudaSuccess) ds.err = topk_gb300::cta512::prepare_device();
     if (ds.err == cudaSuccess) ds.err = topk_gb300::cta256::prepare_device();
+    // a failed query leaves the count unknown (the split then ignores it)
+    if (ds.err == cudaSuccess) {
+      if (topk_gb300::cta512::max_active_clusters(4, &ds.clusters4) != cudaSuccess) ds.clusters4 = 0;
+      if (topk_gb300::cta512::max_active_clusters(8, &ds.clusters8) != cudaSuccess) ds.clusters8 = 0;
+      if (topk_gb300::cta512::max_active_clusters(16, &ds.clusters16) != cudaSuccess) ds.clusters16 = 0;
+      (void)cudaGetLastError();  // a failed query leaves no sticky error
+    }
   });
   if (ds.err != cudaSuccess) return fail_cuda(ds.err);
   *out = &ds;
@@ -232,7 +250,7 @@ int run_one(const topk_problem_t& q, void* workspace, size_t workspace_bytes, cu
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != TOPK_OK) return st;
-  const int g = choose_split(p.batch, hint, ds->sm_count);
+  const int g = choose_split(p.batch, hint, *ds);
   if (static_cast<int64_t>(p.batch) * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
   apply_settings(settings(), &p);
   cudaError_t e;
@@ -407,7 +425,7 @@ int topk_transform_grouped(const topk_problem_t* problems, int32_t n_problems,
       hint = (hint < 0 || hints[i] <= 0) ? -1 : (hints[i] > hint ? hints[i] : hint);
       ++gp.n;
     }
-    const int g = choose_split(rows, hint < 0 ? 0 : hint, ds->sm_count);
+    const int g = choose_split(rows, hint < 0 ? 0 : hint, *ds);
     if (rows * g > INT_MAX) return TOPK_ERR_INVALID_ARGUMENT;
     gp.row_begin[gp.n] = static_cast<int32_t>(rows);
     int32_t k_max = 0;

@@ -139,6 +139,7 @@ struct Ctl {
   uint32_t ns;                        // valid sample size (CTA 0)
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
+  uint32_t skip_fast;                 // the sample predicts an overflowing filter, broadcast
   uint32_t sup[32];                   // super-bin sums of the histogram being searched
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
   uint32_t xt[kMaxCluster];           // per-CTA threshold-bin elements
@@ -721,7 +722,8 @@ template <class Smp>
 __device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s, bool prefetched,
                                                   int32_t L, uint32_t k, int G, int rank,
                                                   uint32_t* hist, uint32_t* mhist, Ctl& ctl,
-                                                  uint32_t* shift2) {
+                                                  uint32_t* shift2, uint32_t cap = 0xFFFFFFFFu,
+                                                  bool predict = false) {
   constexpr int kSampleQuads = Smp::kQuads;
   const int tid = threadIdx.x;
   const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
@@ -832,15 +834,27 @@ __device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s,
         const int bits = 64 - __clzll(static_cast<long long>(gap));
         ctl.lambda = lam;
         ctl.lambda_shift = static_cast<uint32_t>(max(0, bits - (kCandBits - 1)));
+        // (predict) the sample keys at or above lambda, scaled to the row: the filter's
+        // expected candidate count. Far over the buffer (scores packed into a few
+        // values), the filter pass would only find that out: the row goes to the exact
+        // tier at once.
+        if (predict) {
+          const uint32_t at_or_above = win_above + ctl.sel_above + ctl.sel_count;
+          const float expect = __fdividef(static_cast<float>(at_or_above) * static_cast<float>(L),
+                                          static_cast<float>(max(ctl.ns, 1u)));
+          ctl.skip_fast = expect > 2.0f * static_cast<float>(cap) ? 1u : 0u;
+        }
       } else {
         ctl.lambda = 0;
         ctl.lambda_shift = 32 - kCandBits;
+        if (predict) ctl.skip_fast = 0;
       }
     }
     __syncwarp();
     if (G > 1 && tid > 0 && tid < G) {
       dsmem_st(map_rank(smem_addr(&ctl.lambda), tid), ctl.lambda);
       dsmem_st(map_rank(smem_addr(&ctl.lambda_shift), tid), ctl.lambda_shift);
+      if (predict) dsmem_st(map_rank(smem_addr(&ctl.skip_fast), tid), ctl.skip_fast);
     }
   }
   if (G > 1)
@@ -2181,51 +2195,57 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   // ---------------- fast tier
   if (p.use_filter) {
     uint32_t shift2 = 32 - kCandBits;  // rows that skip the sample: the top key bits
+    // rows split over a cluster (the long rows of the adversarial workloads) let the
+    // sample predict an overflowing filter; single-CTA rows measured slower with the check
+    constexpr bool kPredict = (F & kSingle) == 0;
     const uint32_t lambda =
         sampled ? sample_lambda(sm, s, sample_loaded, L, static_cast<uint32_t>(k), G, rank, hist,
-                                mhist, ctl, &shift2)
+                                mhist, ctl, &shift2, cap, kPredict)
                 : 0u;
-    if constexpr (form_of(F) == kPaged) {
-      if (pages > 0) {
-        cp_async_wait_all();
-        m.pt_smem = pt_smem;  // visible to all threads after the next barrier
+    if (!(kPredict && sampled && ctl.skip_fast != 0u)) {  // else the exact tier at once
+      if constexpr (form_of(F) == kPaged) {
+        if (pages > 0) {
+          cp_async_wait_all();
+          m.pt_smem = pt_smem;  // visible to all threads after the next barrier
+        }
+      }
+      uint32_t n_cand;
+      uint32_t* chist = hist + kHC;
+      if (G == 1) {
+        constexpr bool kKeys = (F & kKeysInFilter) != 0;
+        if (lambda >= 0x80000000u)
+          filter_positions<true, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
+        else
+          filter_positions<false, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
+        __syncthreads();
+        n_cand = ctl.cand_cnt;
+        if (!kKeys && n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
+          fill_candidates(rowp, buf, n_cand, lambda, shift2, chist, ctl);
+      } else {
+        const bool remote = rank != 0;
+        const uint32_t buf_remote = map_rank(smem_addr(buf), 0);
+        const uint32_t cnt_remote = map_rank(smem_addr(&ctl.cand_cnt), 0);
+        if (lambda >= 0x80000000u)
+          filter_candidates<true>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap, chist,
+                                  ctl);
+        else
+          filter_candidates<false>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap,
+                                   chist, ctl);
+        cluster_sync();  // every candidate is in CTA 0's buffer; the counter is final
+        if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
+        merge_into_cta0(chist, mhist + kHC, kCandWords);  // ends with a cluster barrier
+        n_cand = ctl.n_cand;
+        chist = mhist + kHC;
+      }
+      if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
+        if (rank == 0)
+          select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
+                               hist, reinterpret_cast<int32_t*>(hist), L, out, m, ctl);
+        return;
       }
     }
-    uint32_t n_cand;
-    uint32_t* chist = hist + kHC;
-    if (G == 1) {
-      constexpr bool kKeys = (F & kKeysInFilter) != 0;
-      if (lambda >= 0x80000000u)
-        filter_positions<true, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
-      else
-        filter_positions<false, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
-      __syncthreads();
-      n_cand = ctl.cand_cnt;
-      if (!kKeys && n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
-        fill_candidates(rowp, buf, n_cand, lambda, shift2, chist, ctl);
-    } else {
-      const bool remote = rank != 0;
-      const uint32_t buf_remote = map_rank(smem_addr(buf), 0);
-      const uint32_t cnt_remote = map_rank(smem_addr(&ctl.cand_cnt), 0);
-      if (lambda >= 0x80000000u)
-        filter_candidates<true>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap, chist,
-                                ctl);
-      else
-        filter_candidates<false>(s, lambda, shift2, buf, buf_remote, cnt_remote, remote, cap,
-                                 chist, ctl);
-      cluster_sync();  // every candidate is in CTA 0's buffer; the counter is final
-      if (rank == 0 && tid < G) dsmem_st(map_rank(smem_addr(&ctl.n_cand), tid), ctl.cand_cnt);
-      merge_into_cta0(chist, mhist + kHC, kCandWords);  // ends with a cluster barrier
-      n_cand = ctl.n_cand;
-      chist = mhist + kHC;
-    }
-    if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
-      if (rank == 0)
-        select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
-                             hist, reinterpret_cast<int32_t*>(hist), L, out, m, ctl);
-      return;
-    }
-    // too few (lambda above the k-th key) or too many candidates: exact tier
+    // too few (lambda above the k-th key) or too many candidates, or too many expected:
+    // exact tier
     for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
     if (G > 1) {
       if (rank == 0)
@@ -2772,6 +2792,21 @@ cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, topk_split_select_kernel<F>, p);
 }
 
+cudaError_t max_active_clusters(int g, int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = rows_smem_bytes(g, kTieCapMax);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(g);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, topk_rows_kernel<kForm>, &cfg);
+}
+
 cudaError_t sort_rows(const Params& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
@@ -2847,6 +2882,8 @@ cudaError_t launch_split(Form form, const Params& p, cudaStream_t stream) {
   }
   return cudaErrorInvalidValue;
 }
+
+cudaError_t max_active_clusters(int g, int* n) { return raw::max_active_clusters(g, n); }
 
 cudaError_t sort_rows(Form form, const Params& p, cudaStream_t stream) {
   switch (form) {

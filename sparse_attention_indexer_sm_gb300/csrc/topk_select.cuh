@@ -98,6 +98,8 @@ constexpr int kTieCap256 = 3072;
   /* Enqueue the chip-wide split (p.split_*: set; no values or sorted output): */        \
   /* batch * split_s filter CTAs, then one select CTA per row. */                       \
   cudaError_t launch_split(Form form, const Params& p, cudaStream_t stream);             \
+  /* Clusters of g CTAs (at the largest tie capacity) the device holds at once. */       \
+  cudaError_t max_active_clusters(int g, int* n);                                       \
   /* The count of failed internal consistency checks on the current device (a */       \
   /* synchronous read), and its reset. */                                               \
   cudaError_t guard_hits(unsigned int* hits);                                           \
@@ -113,6 +115,7 @@ constexpr int kTieCap256 = 3072;
                            int staged, cudaStream_t stream);                            \
   cudaError_t sort_rows(const Params& p, cudaStream_t stream);                          \
   cudaError_t launch_split(const Params& p, cudaStream_t stream);                       \
+  cudaError_t max_active_clusters(int g, int* n);                                       \
   cudaError_t guard_hits(unsigned int* hits);                                           \
   cudaError_t reset_guard_hits();
 
