@@ -727,7 +727,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s,
   constexpr int kSampleQuads = Smp::kQuads;
   const int tid = threadIdx.x;
   const bool finder = rank == 0 && tid < 32;  // the warp that finds the thresholds
-  // round 1: coarse bins (top 10 key bits), one shared atomic per sample key (this
+  // first sample round: coarse bins (top 10 key bits), one shared atomic per sample key (this
   // measured faster than first aggregating a warp's equal bins with a match). The
   // valid sample size goes to CTA 0.
   uint32_t mine = 0;
@@ -805,7 +805,7 @@ __device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s,
   else
     __syncthreads();
 
-  // round 2: fine bins over [win_lo, end of coarse bin sel2_t]
+  // second sample round: fine bins over [win_lo, end of coarse bin sel2_t]
   const uint32_t win_lo = ctl.win_lo, f = ctl.win_shift, win_above = ctl.win_above;
   const uint64_t span =
       (static_cast<uint64_t>(ctl.sel2_t + 1) << (32 - kFastBits)) - static_cast<uint64_t>(win_lo);
@@ -1724,7 +1724,7 @@ __device__ __forceinline__ void filter_pass(const uint4* stage, int slot0, int c
 // The second sample round of staged_lambda (every thread; the same sample quad v at
 // row position j, `in` as there): 1024 equal key bins over [wlo, whi] (keys above
 // it counted apart) in chist's region, which is cleared again afterwards. Returns
-// lambda and sets *shift; when rs falls above the window (rounding), round 1's
+// lambda and sets *shift; when rs falls above the window (rounding), the first round's
 // (wlo, shift1) stands. Kept out of line, as it runs only for scores packed into a
 // narrow band.
 __device__ __noinline__ uint32_t staged_refine(uint4 v, int32_t j, bool in, int32_t L, uint32_t rs,
@@ -1745,7 +1745,7 @@ __device__ __noinline__ uint32_t staged_refine(uint4 v, int32_t j, bool in, int3
   }
   above = __reduce_add_sync(kFull, above);
   if (lane == 0) ctl.wcnt[warp] = above;
-  __syncthreads();  // (also: every thread has read round 1's bins)
+  __syncthreads();  // (also: every thread has read the first round's bins)
   uint32_t na = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) na += ctl.wcnt[w];
@@ -1802,7 +1802,7 @@ __device__ __forceinline__ uint32_t staged_lambda(const uint4& v, int32_t j, boo
   const uint32_t M = __reduce_max_sync(kFull, own ? ctl.wmax[lane] : 0u);
   const uint32_t Mn = __reduce_min_sync(kFull, own ? ctl.wmin[lane] : 0xFFFFFFFFu);
   const uint32_t ns = __reduce_add_sync(kFull, own ? ctl.wcnt[lane] : 0u);
-  // round 1: log bins of the distance in value from the largest sample element, in
+  // first sample round: log bins of the distance in value from the largest sample element, in
   // the 32 powers of two below the sample's range (index 1023 - bin, so that larger
   // scores have higher indices); distances past the window share its end bins
   const float Mv = __uint_as_float(key_bits(M));
