@@ -264,6 +264,9 @@ int run_one(const topk_problem_t& q, void* workspace, size_t workspace_bytes, cu
     p.split_s = plan.parts;
     p.split_cap = plan.cap;
     p.gather_cap = plan.gather_cap;
+    // the select kernel's cluster: the row split the clusters would take (its exact tier
+    // runs there when a row's candidates do not fit)
+    p.split_g = std::max(g, 1);
     e = topk_gb300::cta512::launch_split(static_cast<Form>(q.form), p, stream);
     return e == cudaSuccess ? TOPK_OK : fail_cuda(e);
   }

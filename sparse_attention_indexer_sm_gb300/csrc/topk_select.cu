@@ -2379,20 +2379,26 @@ __device__ __forceinline__ void split_filter_part(const Params& p, int row, int 
   }
 }
 
-// The select CTA of row `row`: gathers the filter CTAs' candidates (and their
-// histogram) and selects; shared memory as row_body's for one CTA, with a buffer of
-// gather_cap candidates.
+// The select cluster of row `row` (G CTAs, this one `rank`): CTA 0 gathers the filter
+// CTAs' candidates (and their histogram) and selects, the others end; a row whose
+// candidates did not fit, or fell short of k, runs the exact tier on the whole cluster
+// (every CTA reads the same counts, so all take the same branch). Shared memory as
+// row_body's for a cluster of G, with a buffer of gather_cap candidates.
 template <int F>
-__device__ __forceinline__ void split_select_row(const Params& p, int row, uint32_t* dyn, Ctl& ctl) {
+__device__ __forceinline__ void split_select_row(const Params& p, int row, int G, int rank,
+                                                 uint32_t* dyn, Ctl& ctl) {
   const int tid = threadIdx.x;
   const int S = p.split_s;
   uint32_t* hist = dyn;
   uint2* list = reinterpret_cast<uint2*>(dyn + kHistWords);
   int32_t* pt_smem = reinterpret_cast<int32_t*>(dyn + kHistWords + kListWords);
-  uint2* buf = reinterpret_cast<uint2*>(dyn + kHistWords + kListWords + kPtCap);
+  uint32_t* mhist = dyn + kHistWords + kListWords + kPtCap;
+  uint2* buf = reinterpret_cast<uint2*>(dyn + (G > 1 ? 2 : 1) * kHistWords + kListWords + kPtCap);
   const uint32_t gcap = static_cast<uint32_t>(p.gather_cap);
   allow_next_grid();
   for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
+  if (G > 1 && rank == 0)
+    for (int i = tid; i < kHistWords; i += kThreads) mhist[i] = 0;
   if (tid == 0) {
     ctl.win_cnt = 0;
     ctl.tie_cnt = 0;
@@ -2418,21 +2424,25 @@ __device__ __forceinline__ void split_select_row(const Params& p, int row, uint3
   int32_t* out = p.out + static_cast<int64_t>(row) * k;
   if constexpr (form_of(F) == kPaged) {
     const int64_t up = static_cast<int64_t>(L) + p.page_size - 1;
-    if ((p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size) > p.pt_stride && tid == 0)
+    if ((p.page_shift >= 0 ? up >> p.page_shift : up / p.page_size) > p.pt_stride && tid == 0 &&
+        rank == 0)
       guard_hit();
   }
+  // CTA 0, which writes the selection, stages the page table
   int32_t pages = 0;
   if constexpr (form_of(F) == kPaged) {
-    if (m.pt_n <= kPtCap) {
+    if (rank == 0 && m.pt_n <= kPtCap) {
       pages = m.pt_n;
       for (int32_t i = tid; i < pages; i += kThreads) cp_async4(pt_smem + i, m.pt_row + i);
     }
   }
-  if (L <= k) {
+  if (L <= k) {  // each CTA writes its share of the slots
     cp_async_wait_all();
     __syncthreads();
     if (pages > 0) m.pt_smem = pt_smem;
-    for (int32_t i = tid; i < k; i += kThreads) {
+    const int32_t s0 = static_cast<int32_t>(static_cast<int64_t>(k) * rank / G);
+    const int32_t s1 = static_cast<int32_t>(static_cast<int64_t>(k) * (rank + 1) / G);
+    for (int32_t i = s0 + tid; i < s1; i += kThreads) {
       if (i < L)
         emit<F>(out, k, static_cast<uint32_t>(i), m, i, 0u);
       else
@@ -2447,20 +2457,23 @@ __device__ __forceinline__ void split_select_row(const Params& p, int row, uint3
   uint32_t total = 0;
   const uint32_t off = block_excl_scan(static_cast<uint32_t>(c), ctl, &total);
   const bool over = __syncthreads_or(static_cast<uint32_t>(c) > scap) != 0;
+  if (__builtin_expect(over || total < static_cast<uint32_t>(k) || total > gcap, 0)) {
+    // exact tier over the whole row on the cluster (hist and, for CTA 0, mhist are zero)
+    if (G > 1)
+      cluster_sync();  // every CTA running, its histograms cleared
+    else
+      __syncthreads();
+    exact_tier<F>(make_slice(rowp, L, rank, G), L, k, out, m, pages, pt_smem, G, rank, hist, mhist,
+                  buf, min(gcap, static_cast<uint32_t>(kTieCapMax)), ctl);
+    return;
+  }
+  if (rank != 0) return;  // CTA 0 selects
   int32_t* part_off = reinterpret_cast<int32_t*>(list);  // S + 1 offsets, then the scan is read
   if (tid < S) part_off[tid] = static_cast<int32_t>(off);
   if (tid == 0) part_off[S] = static_cast<int32_t>(total);
   cp_async_wait_all();
   __syncthreads();
   if (pages > 0) m.pt_smem = pt_smem;
-  if (__builtin_expect(over || total < static_cast<uint32_t>(k) || total > gcap, 0)) {
-    // exact tier over the whole row on this CTA
-    for (int i = tid; i < kHistWords; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    exact_tier<F>(make_slice(rowp, L, 0, 1), L, k, out, m, pages, pt_smem, 1, 0, hist, nullptr, buf,
-                  min(gcap, static_cast<uint32_t>(kTieCapMax)), ctl);
-    return;
-  }
   const uint32_t lambda = lh.x, shift = lh.y;
   uint32_t* chist = hist + kHC;
   // gather: kThreads / S threads per part, each taking every (kThreads / S)-th entry
@@ -2546,10 +2559,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_split_filter_kernel
   split_filter_part<F>(p, static_cast<int>(blockIdx.x) / S, static_cast<int>(blockIdx.x) % S, dyn, ctl);
 }
 template <int F>
-__global__ void __launch_bounds__(kThreads) topk_split_select_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) topk_split_select_kernel(const Params p) {
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Ctl ctl;
-  split_select_row<F>(p, static_cast<int>(blockIdx.x), dyn, ctl);
+  const int G = static_cast<int>(cluster_nctarank());
+  split_select_row<F>(p, static_cast<int>(blockIdx.x) / G, G, static_cast<int>(cluster_ctarank()),
+                      dyn, ctl);
 }
 
 // The sort pass of the sorted output (one CTA per row, after the selection kernel):
@@ -2721,7 +2736,7 @@ cudaError_t prepare_device() {
   if (e == cudaSuccess)
     e = prepare_kernel(topk_split_filter_kernel<F>, split_filter_smem_bytes(kSplitCapMax));
   if (e == cudaSuccess)
-    e = prepare_kernel(topk_split_select_kernel<F>, rows_smem_bytes(1, kGatherCapMax));
+    e = prepare_kernel(topk_split_select_kernel<F>, rows_smem_bytes(2, kGatherCapMax));
   if constexpr (kHasStaged) {
     const size_t full = staged_smem_bytes<false>(kTieCapMax), half = staged_smem_bytes<true>(kTieCapMax);
     if (e == cudaSuccess) e = prepare_kernel(topk_rows_kernel<F | kSingle | kStaged>, full);
@@ -2771,7 +2786,8 @@ cudaError_t launch_group(const GroupParams& gp, int g, bool opts, bool keys_in_f
 cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   constexpr int F = kForm;
   if (p.split_s < 1 || p.split_s > kMaxSplit || (p.split_s & (p.split_s - 1)) != 0 ||
-      p.split_cap < 0 || p.split_cap > kSplitCapMax || p.gather_cap < 0 ||
+      p.split_cap < 0 || p.split_cap > kSplitCapMax || p.gather_cap < 0 || p.split_g < 1 ||
+      p.split_g > kMaxCluster || (p.split_g & (p.split_g - 1)) != 0 ||
       p.gather_cap > kGatherCapMax || p.split_ws == nullptr || p.values != nullptr ||
       p.staged != nullptr)
     return cudaErrorInvalidValue;
@@ -2787,8 +2803,17 @@ cudaError_t launch_split(const Params& p, cudaStream_t stream) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, topk_split_filter_kernel<F>, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 1, 1);
-  cfg.dynamicSmemBytes = rows_smem_bytes(1, p.gather_cap);
+  // the select kernel: one cluster of split_g CTAs per row
+  cudaLaunchAttribute attr2[2];
+  attr2[0] = attr[0];
+  attr2[1].id = cudaLaunchAttributeClusterDimension;
+  attr2[1].val.clusterDim.x = static_cast<unsigned>(p.split_g);
+  attr2[1].val.clusterDim.y = 1;
+  attr2[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(p.batch) * p.split_g), 1, 1);
+  cfg.dynamicSmemBytes = rows_smem_bytes(p.split_g, p.gather_cap);
+  cfg.attrs = attr2;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk_split_select_kernel<F>, p);
 }
 

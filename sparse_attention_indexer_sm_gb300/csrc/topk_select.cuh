@@ -38,6 +38,7 @@ struct Params {
   int32_t split_s;             // CTAs per row: a power of two, at most kMaxSplit
   int32_t split_cap;           // candidates one filter CTA may store
   int32_t gather_cap;          // candidates the select CTA may gather
+  int32_t split_g;             // CTAs of the select cluster (its exact tier's row split)
 };
 
 // The chip-wide split's workspace for `rows` rows of `s` CTAs storing up to `cap`

@@ -197,6 +197,16 @@ def test_chip_split_forms(pkg, form, k):
     assert_parity(w, got)
 
 
+@pytest.mark.parametrize("dist", ["banded", "narrow", "subnormal"])
+def test_chip_split_exact_tier_on_clusters(pkg, dist):
+    """Long concentrated rows through the chip-wide split (automatic for 4 rows): their
+    candidates overflow the per-CTA stores, so the select kernel's cluster runs the exact
+    tier over each row."""
+    w = _mixed(940, dist, batch=4, stride=100003, k=2048)
+    assert pkg.topk_workspace_bytes(w.batch, w.scores.shape[1], w.k) > 0
+    assert_parity(w, run_gpu(pkg, w), check_rows=2)
+
+
 def test_chip_split_workspace(pkg):
     """A caller's workspace, reused without initialisation, gives the same rows; one
     too small sends the call to the cluster path, with the same result."""
