@@ -17,9 +17,10 @@
 //                of the top 10 key bits (summed over the cluster through distributed
 //                shared memory) finds the coarse bins of both; a second 1024-bin
 //                histogram spanning just those coarse bins resolves them: lambda is the
-//                lower edge of r_s's fine bin, lambda_hi the upper edge of r_lo's. One
-//                warp finds each threshold. Rows that fit the candidate buffer skip the
-//                sample (lambda = 0).
+//                lower edge of r_s's fine bin, lambda_hi the upper edge of r_lo's. Every
+//                thread takes part in each threshold search. Rows that fit the candidate
+//                buffer skip the sample (lambda = 0); cluster rows whose sample predicts
+//                far more candidates than the buffer holds go to the exact tier at once.
 //  F2. filter    one streaming pass with 128-bit loads compares every raw fp32 bit
 //                pattern with lambda (a single integer compare: for lambda in the
 //                non-negative range a signed compare, otherwise an unsigned one,
@@ -36,7 +37,8 @@
 //                element of the exact top-k is among them (they hold k elements with
 //                key >= lambda, so the k-th key is >= lambda). CTA 0 finds the
 //                threshold bin of the candidate histogram, writes the candidates above
-//                it, and orders the candidates of that bin on the 64-bit composite
+//                it (through output slots in shared memory, written out at the end),
+//                and orders the candidates of that bin on the 64-bit composite
 //                (key, ~position), so equal keys go to the smaller position: by a rank
 //                count spread over the CTA up to 256 of them, by radix rounds beyond.
 //                Otherwise the exact tier runs.
@@ -55,8 +57,16 @@
 //                takes its quota of equal elements by a block-wide prefix count (the
 //                page's overflow rescan): nothing is ever dropped.
 //
-// No step waits on another CTA except through the hardware cluster barrier: no
-// spin loop, no global workspace, one launch per call.
+// Two more paths share these steps (each described at its code): the staged tier
+// (single-CTA rows of 16384 to 32768 elements, 64 rows up to one per SM: the row is
+// copied into shared memory from kernel start and lambda comes from one sample round
+// in value space) and the chip-wide split (batches of 4 rows up to one per 16 SMs of
+// rows of 65536 elements or more: many CTAs per row filter into a caller workspace,
+// one cluster per row then selects).
+//
+// No step waits on another CTA except through the hardware cluster barrier or the
+// grid dependency between launches: no spin loop. One launch per call (two for the
+// chip-wide split, whose workspace the caller provides).
 
 #include <cstdint>
 
