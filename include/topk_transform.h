@@ -35,8 +35,9 @@
  * Memory and ownership: every pointer argument is device memory owned by the
  * caller (for example torch tensors passed as data_ptr()). The library never
  * allocates, frees or synchronises; each call enqueues one kernel on `stream`
- * (NULL = the legacy default stream) and returns. All inputs must stay valid and
- * unmodified until that kernel has finished. `out` is fully written, including
+ * (NULL = the legacy default stream; two kernels for a call that takes the
+ * chip-wide split, see topk_workspace_bytes) and returns. All inputs must stay
+ * valid and unmodified until the call's kernels have finished. `out` is fully written, including
  * the -1 padding, so it need not be pre-filled. The first call on a device sets
  * kernel attributes on that device; make it before capturing a CUDA graph.
  *
