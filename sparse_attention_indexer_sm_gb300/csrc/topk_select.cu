@@ -1170,6 +1170,18 @@ __device__ __forceinline__ void select_in_buffer(const uint2* buf, uint32_t c, u
 template <int F>
 __device__ __forceinline__ void write_slots(const int32_t* slots, uint32_t upto, int32_t L,
                                             int32_t* out, const OutMap& m) {
+  if constexpr (form_of(F) == kPaged) {
+    if (m.pt_smem != nullptr && m.ps_shift >= 0) {  // the usual case, with no branch per slot
+      const int32_t sh = m.ps_shift, msk = m.ps - 1;
+      for (uint32_t i = threadIdx.x; i < upto; i += kThreads) {
+        const int32_t j = slots[i];
+        const int32_t page = j >> sh;
+        const bool ok = static_cast<uint32_t>(j) < static_cast<uint32_t>(L) && page < m.pt_n;
+        out[i] = ok ? m.pt_smem[page] * m.ps + (j & msk) : -1;
+      }
+      return;
+    }
+  }
   for (uint32_t i = threadIdx.x; i < upto; i += kThreads) {
     const int32_t j = slots[i];
     out[i] = static_cast<uint32_t>(j) < static_cast<uint32_t>(L) ? map_pos<F>(m, j) : -1;
@@ -1236,24 +1248,20 @@ __device__ __forceinline__ void select_candidates(const uint2* buf, uint32_t n, 
     const uint32_t sw = lane < kWarps ? ctl.scan[lane] : 0u;
     const uint32_t first = run + __reduce_add_sync(kFull, lane < warp ? sw : 0u) + x - mine;
     run += __reduce_add_sync(kFull, sw);
-    uint32_t ws = first & 0xFFFFu, ts = first >> 16;
+    // entry r's slot: the first slot plus this thread's entries of its kind before r;
+    // stores predicated on the entry's kind, the slots' bounds counted afterwards
+    const uint32_t ws = first & 0xFFFFu, ts = first >> 16;
 #pragma unroll
     for (int r = 0; r < kClsR; ++r) {
-      if ((wb >> r) & 1u) {
-        if (ws < above)
-          put(ws, e[r]);
-        else
-          guard_hit();
-        ++ws;
-      }
-      if ((tb >> r) & 1u) {
-        if (ts < ct)
-          list[ts] = e[r];
-        else
-          guard_hit();
-        ++ts;
-      }
+      const uint32_t below = (1u << r) - 1u;
+      const uint32_t wr = ws + static_cast<uint32_t>(__popc(wb & below));
+      const uint32_t tr = ts + static_cast<uint32_t>(__popc(tb & below));
+      if (((wb >> r) & 1u) != 0u && wr < above) put(wr, e[r]);
+      if (((tb >> r) & 1u) != 0u && tr < ct) list[tr] = e[r];
     }
+    // slots past the bin's counts (only if the scores changed under the kernel)
+    if (wb != 0u && ws + static_cast<uint32_t>(__popc(wb)) > above) guard_hit();
+    if (tb != 0u && ts + static_cast<uint32_t>(__popc(tb)) > ct) guard_hit();
     if (base + static_cast<uint32_t>(kClsR * kThreads) < n) __syncthreads();  // ctl.scan again
   }
   __syncthreads();
