@@ -886,6 +886,24 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
     return bits <= thr;
 }
 
+// The candidate histogram (bin = min((key - lambda) >> shift, kCandBins - 1)) of the
+// n candidates in buf, counted by every thread (chist zero on entry; a barrier at the
+// end). Counting it in the filters' per-candidate loops measured slower.
+__device__ __forceinline__ void count_candidates(const uint2* buf, uint32_t n, uint32_t lambda,
+                                                 uint32_t shift, uint32_t* chist) {
+  uint32_t top = 0;  // the last bin, counted per warp
+  for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t d = (buf[i].x - lambda) >> shift;
+    if (d >= static_cast<uint32_t>(kCandBins - 1))
+      ++top;
+    else
+      atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
+  }
+  top = __reduce_add_sync(kFull, top);
+  if ((threadIdx.x & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
+  __syncthreads();
+}
+
 // F2, a row owned by one CTA: stream the row, keep per lane a 32-bit candidate
 // mask per iteration (8 quads), and every MI iterations turn the masks into
 // candidates written compactly into the buffer at slots from one reservation per
@@ -894,13 +912,11 @@ __device__ __forceinline__ bool is_candidate(uint32_t bits, uint32_t thr) {
 // positions are written (entry .y; fill_candidates reads the values back from L2
 // afterwards); with kKeys the loads keep their lines in L1, the masks are decoded
 // every iteration (MI = 1) and each candidate's value is read back from L1 at
-// once: the entry gets its key and the candidate histogram `chist` (bin =
-// min((key - lambda) >> shift, kCandBins - 1); zero on entry) its count. Slots at
-// or beyond `cap` are counted but not written.
+// once, so the entry gets its key (its histogram comes from count_candidates).
+// Slots at or beyond `cap` are counted but not written.
 template <bool kPos, bool kKeys>
-__device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint32_t shift,
-                                                 uint2* buf, uint32_t cap, uint32_t* chist,
-                                                 Ctl& ctl) {
+__device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda, uint2* buf,
+                                                 uint32_t cap, Ctl& ctl) {
   const int tid = threadIdx.x;
   const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
   constexpr int U = kFilterUnroll;
@@ -908,7 +924,6 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
   constexpr int32_t kStep = U * kThreads;
   int32_t ej;
   const bool edge = edge_position(s, &ej) && is_candidate<kPos>(__float_as_uint(s.row[ej]), thr);
-  uint32_t top = 0;  // kKeys: candidates in the last candidate-histogram bin
   bool first = true;
   for (int32_t gbase = 0; first || gbase < s.nq; gbase += MI * kStep) {
     uint32_t mk[MI];
@@ -944,11 +959,6 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
       auto put = [&](int32_t j) {
         if constexpr (kKeys) {
           const uint32_t key = order_key(__float_as_uint(__ldg(s.row + j)));  // from L1
-          const uint32_t d = (key - lambda) >> shift;
-          if (d >= static_cast<uint32_t>(kCandBins - 1))
-            ++top;
-          else
-            atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
           if (slot < cap) buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
         } else {
           if (slot < cap) buf[slot].y = static_cast<uint32_t>(j);
@@ -968,11 +978,6 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
       }
     }
     first = false;
-  }
-  if constexpr (kKeys) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
-    if ((tid & 31) == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
   }
 }
 
@@ -1557,7 +1562,8 @@ __device__ __forceinline__ void exact_tier(const Slice& s, int32_t L, int32_t k,
 //     exact candidates; each thread reads back only what it copied itself, so no
 //     barrier is needed;
 //   - each warp reserves its candidates' slots once per pass and writes their keys
-//     and positions into the candidate buffer and histogram.
+//     and positions into the candidate buffer; the candidate histogram is counted
+//     from the buffer once the filter is done.
 // For the raw and paged forms the copies cover the whole row stride and go out
 // before the row's length has arrived; elements at or past it are ignored.
 // Lambda comes from one round over the sample: the distance d = M - x in value of
@@ -1613,18 +1619,11 @@ __device__ __forceinline__ uint32_t quad_elem(const uint4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
-// One candidate: its key into the buffer at `slot` (if below cap) and into the
-// candidate histogram; the last bin is counted per lane (top).
-__device__ __forceinline__ void staged_put(uint32_t bits, int32_t j, uint32_t slot, uint32_t lambda,
-                                           uint32_t shift, uint2* buf, uint32_t cap,
-                                           uint32_t* chist, uint32_t& top) {
-  const uint32_t key = order_key(bits);
-  const uint32_t d = (key - lambda) >> shift;
-  if (d >= static_cast<uint32_t>(kCandBins - 1))
-    ++top;
-  else
-    atomicAdd(&chist[hist_index(static_cast<int>(d))], 1u);
-  if (slot < cap) buf[slot] = make_uint2(key, static_cast<uint32_t>(j));
+// One candidate of the staged tier's filter: its key and position into the buffer at
+// `slot` (if below cap); the candidate histogram is counted from the buffer afterwards.
+__device__ __forceinline__ void staged_put_key(uint32_t bits, int32_t j, uint32_t slot, uint2* buf,
+                                               uint32_t cap) {
+  if (slot < cap) buf[slot] = make_uint2(order_key(bits), static_cast<uint32_t>(j));
 }
 
 // Candidate mask of quad v, quad q of the body whose first element is at row
@@ -1701,13 +1700,13 @@ __device__ __forceinline__ bool quad_may(const uint4& v, uint32_t thr) {
 // the chunk's copy group has landed (kLater groups were committed after the pass);
 // then the flagged quads, about one in five, are read again for their exact
 // candidates (positions below L), which go with this thread's edge element (when
-// `edge`) to buf / chist at slots from one reservation per warp on ctl.cand_cnt.
+// `edge`) to buf, as (key, position), at slots from one reservation per warp on
+// ctl.cand_cnt.
 template <bool kPos, int kLater>
 __device__ __forceinline__ void filter_pass(const uint4* stage, int slot0, int c0, int32_t nvec,
                                             int32_t head, int32_t L, bool edge, int32_t ej,
-                                            uint32_t ebits, uint32_t lambda, uint32_t shift,
-                                            uint2* buf, uint32_t cap, uint32_t* chist,
-                                            uint32_t& top, Ctl& ctl) {
+                                            uint32_t ebits, uint32_t lambda, uint2* buf,
+                                            uint32_t cap, Ctl& ctl) {
   const int tid = threadIdx.x;
   const uint32_t thr = kPos ? (lambda ^ 0x80000000u) : ~lambda;
   uint32_t fl = 0;  // bit i: this thread's quad of pass chunk i may hold a candidate
@@ -1728,14 +1727,14 @@ __device__ __forceinline__ void filter_pass(const uint4* stage, int slot0, int c
   const bool ec = edge && is_candidate<kPos>(ebits, thr);
   uint32_t slot = warp_reserve(&ctl.cand_cnt, 0u, false,
                                static_cast<uint32_t>(__popc(m)) + (ec ? 1u : 0u));
-  if (ec) staged_put(ebits, ej, slot++, lambda, shift, buf, cap, chist, top);
+  if (ec) staged_put_key(ebits, ej, slot++, buf, cap);
   while (m != 0u) {
     const int bit = __ffs(m) - 1;
     m &= m - 1u;
     const int i = bit >> 2, e = bit & 3;
     const int32_t q = (c0 + i) * kChunkQuads + tid;
-    staged_put(quad_elem(stage[(slot0 + i) * kChunkQuads + tid], e), head + 4 * q + e, slot++, lambda,
-               shift, buf, cap, chist, top);
+    staged_put_key(quad_elem(stage[(slot0 + i) * kChunkQuads + tid], e), head + 4 * q + e, slot++,
+                   buf, cap);
   }
 }
 
@@ -2029,39 +2028,29 @@ __device__ __forceinline__ void staged_row(const Params& p, int row, uint32_t* d
                            &shift2);
 
   // ---- the second pass's copies, and the filter of each chunk as it lands
-  uint32_t top = 0;
   const bool pos = lambda >= 0x80000000u;
   if constexpr (!kHalf) {  // the whole row in the staging area
     copy_pass(stage, kPassChunks, kPassChunks, vb, nvec);
     if (pos) {
-      filter_pass<true, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf,
-                                     cap, chist, top, ctl);
-      filter_pass<true, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2,
-                           buf, cap, chist, top, ctl);
+      filter_pass<true, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, buf, cap, ctl);
+      filter_pass<true, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda, buf,
+                           cap, ctl);
     } else {
-      filter_pass<false, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf,
-                                      cap, chist, top, ctl);
-      filter_pass<false, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda,
-                            shift2, buf, cap, chist, top, ctl);
+      filter_pass<false, kPassChunks>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, buf, cap, ctl);
+      filter_pass<false, 0>(stage, kPassChunks, kPassChunks, nvec, head, L, false, 0, 0u, lambda, buf,
+                            cap, ctl);
     }
   } else {  // half the row: the second pass into this thread's first-pass slots
     if (pos)
-      filter_pass<true, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf, cap, chist,
-                           top, ctl);
+      filter_pass<true, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, buf, cap, ctl);
     else
-      filter_pass<false, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, shift2, buf, cap,
-                            chist, top, ctl);
+      filter_pass<false, 0>(stage, 0, 0, nvec, head, L, edge, ej, ebits, lambda, buf, cap, ctl);
     copy_pass(stage, 0, kPassChunks, vb, nvec);
     if (pos)
-      filter_pass<true, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2, buf, cap,
-                           chist, top, ctl);
+      filter_pass<true, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, buf, cap, ctl);
     else
-      filter_pass<false, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, shift2, buf,
-                            cap, chist, top, ctl);
+      filter_pass<false, 0>(stage, 0, kPassChunks, nvec, head, L, false, 0, 0u, lambda, buf, cap, ctl);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) top += __shfl_xor_sync(kFull, top, off);
-  if (lane == 0 && top != 0) atomicAdd(&chist[hist_index(kCandBins - 1)], top);
   cp_async_wait_all();  // the page table
   if constexpr (form_of(F) == kPaged) {
     if (pages > 0) m.pt_smem = pt_smem;  // visible to all threads after the barrier below
@@ -2070,7 +2059,11 @@ __device__ __forceinline__ void staged_row(const Params& p, int row, uint32_t* d
   const uint32_t n_cand = ctl.cand_cnt;
   uint2* list = reinterpret_cast<uint2*>(dyn);  // the staging area is free from here on
   uint32_t* scratch = dyn + kListWords;
+  // the candidate histogram, from the buffer
+  if (n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
+    count_candidates(buf, n_cand, lambda, shift2, chist);
   if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
+
     select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list, scratch,
                          reinterpret_cast<int32_t*>(scratch + kHistWords), L, out, m, ctl);
     return;
@@ -2232,13 +2225,16 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
       if (G == 1) {
         constexpr bool kKeys = (F & kKeysInFilter) != 0;
         if (lambda >= 0x80000000u)
-          filter_positions<true, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
+          filter_positions<true, kKeys>(s, lambda, buf, cap, ctl);
         else
-          filter_positions<false, kKeys>(s, lambda, shift2, buf, cap, chist, ctl);
+          filter_positions<false, kKeys>(s, lambda, buf, cap, ctl);
         __syncthreads();
         n_cand = ctl.cand_cnt;
         if (!kKeys && n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
           fill_candidates(rowp, buf, n_cand, lambda, shift2, chist, ctl);
+        if (kKeys && n_cand >= static_cast<uint32_t>(k) && n_cand <= cap)
+          count_candidates(buf, n_cand, lambda, shift2, chist);
+
       } else {
         const bool remote = rank != 0;
         const uint32_t buf_remote = map_rank(smem_addr(buf), 0);
@@ -2383,9 +2379,9 @@ __device__ __forceinline__ void split_filter_part(const Params& p, int row, int 
       sampled ? sample_lambda(sm, s, true, L, static_cast<uint32_t>(k), 1, 0, hist, nullptr, ctl, &shift2)
               : 0u;
   if (lambda >= 0x80000000u)
-    filter_positions<true, true>(s, lambda, shift2, buf, cap, hist + kHC, ctl);
+    filter_positions<true, true>(s, lambda, buf, cap, ctl);
   else
-    filter_positions<false, true>(s, lambda, shift2, buf, cap, hist + kHC, ctl);
+    filter_positions<false, true>(s, lambda, buf, cap, ctl);
   __syncthreads();
   const uint32_t n = ctl.cand_cnt;
   const uint32_t stored = min(n, cap);
