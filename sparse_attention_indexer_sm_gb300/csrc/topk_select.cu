@@ -908,9 +908,11 @@ __device__ __forceinline__ void count_candidates(const uint2* buf, uint32_t n, u
 // mask per iteration (8 quads), and every MI iterations turn the masks into
 // candidates written compactly into the buffer at slots from one reservation per
 // warp and group on the CTA's counter (ctl.cand_cnt, zero on entry). Holding only
-// masks lets the loads of a whole group be in flight together. Without kKeys only
-// positions are written (entry .y; fill_candidates reads the values back from L2
-// afterwards); with kKeys the loads keep their lines in L1, the masks are decoded
+// masks lets the loads of a whole group be in flight together. The loads keep their
+// lines in L1. Without kKeys only positions are written (entry .y; fill_candidates
+// reads the values back afterwards, mostly from L1: keeping the lines there measured
+// 0.5 us faster at one row, against streaming them past L1 and reading back from L2);
+// with kKeys the masks are decoded
 // every iteration (MI = 1) and each candidate's value is read back from L1 at
 // once, so the entry gets its key (its histogram comes from count_candidates).
 // Slots at or beyond `cap` are counted but not written.
@@ -936,7 +938,7 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int32_t q = base + u * kThreads + tid;
-          x[u] = q < s.nq ? (kKeys ? ld_keep(s.vec + q) : ld_stream(s.vec + q))
+          x[u] = q < s.nq ? ld_keep(s.vec + q)
                           : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -982,11 +984,10 @@ __device__ __forceinline__ void filter_positions(const Slice& s, uint32_t lambda
 }
 
 // F2, a row owned by one CTA: the n buffered positions get their keys, read back
-// (from L2) in batches of 2048, and the candidate histogram (bin =
-// min((key - lambda) >> shift, kCandBins - 1)) is counted in `chist`, which is zero
-// on entry. The last
-// bin collects most candidates, so it is counted per warp (ballot) rather than by
-// one shared atomic per candidate.
+// (from L1, where the filter kept the row, or from L2) in batches of 2048, and the
+// candidate histogram (bin = min((key - lambda) >> shift, kCandBins - 1)) is counted
+// in `chist`, which is zero on entry. The last bin collects most candidates, so it is
+// counted per warp (ballot) rather than by one shared atomic per candidate.
 __device__ __forceinline__ void fill_candidates(const float* row, uint2* buf, uint32_t n,
                                                 uint32_t lambda, uint32_t shift,
                                                 uint32_t* chist, Ctl& ctl) {
