@@ -150,6 +150,7 @@ struct Ctl {
   uint32_t win_lo, win_shift, win_above;  // fine sample window (broadcast)
   uint32_t lambda, lambda_shift;      // filter threshold key and bin width, broadcast
   uint32_t skip_fast;                 // the sample predicts an overflowing filter, broadcast
+  uint32_t ex_shift;                  // with skip_fast: the exact tier's first window, broadcast
   uint32_t sup[32];                   // super-bin sums of the histogram being searched
   uint32_t xa[kMaxCluster];           // per-CTA winners (cluster exchange)
   uint32_t xt[kMaxCluster];           // per-CTA threshold-bin elements
@@ -853,18 +854,27 @@ __device__ __forceinline__ uint32_t sample_lambda(const Smp& sm, const Slice& s,
           const float expect = __fdividef(static_cast<float>(at_or_above) * static_cast<float>(L),
                                           static_cast<float>(max(ctl.ns, 1u)));
           ctl.skip_fast = expect > 2.0f * static_cast<float>(cap) ? 1u : 0u;
+          // the exact tier then starts below the bits that lambda and lambda_hi share
+          // (every bit when they are equal: scores packed into a few values)
+          ctl.ex_shift = 32u - static_cast<uint32_t>(__clz(lam ^ static_cast<uint32_t>(hi)));
         }
       } else {
         ctl.lambda = 0;
         ctl.lambda_shift = 32 - kCandBits;
-        if (predict) ctl.skip_fast = 0;
+        if (predict) {
+          ctl.skip_fast = 0;
+          ctl.ex_shift = 32;
+        }
       }
     }
     __syncwarp();
     if (G > 1 && tid > 0 && tid < G) {
       dsmem_st(map_rank(smem_addr(&ctl.lambda), tid), ctl.lambda);
       dsmem_st(map_rank(smem_addr(&ctl.lambda_shift), tid), ctl.lambda_shift);
-      if (predict) dsmem_st(map_rank(smem_addr(&ctl.skip_fast), tid), ctl.skip_fast);
+      if (predict) {
+        dsmem_st(map_rank(smem_addr(&ctl.skip_fast), tid), ctl.skip_fast);
+        dsmem_st(map_rank(smem_addr(&ctl.ex_shift), tid), ctl.ex_shift);
+      }
     }
   }
   if (G > 1)
@@ -1442,11 +1452,16 @@ __device__ __forceinline__ void emit_equal(const Slice& s, uint32_t tau, int32_t
 // a cluster of G). hist and, in CTA 0, mhist are zero on entry; buf holds `cap`
 // (key, position) entries. Paged rows whose table was copied to shared memory
 // (pages > 0 entries at pt_smem) wait for that copy here if nothing waited before.
+// start_shift < 32: the first round looks only at keys whose bits above start_shift
+// equal start_prefix (a window that the sample expects to hold the k-th key), and
+// counts the keys above the window; if the k-th key is not in the window after all,
+// the rounds start again from the top bits. The same value on every CTA of a cluster.
 template <int F>
 __device__ __forceinline__ void exact_tier(const Slice& s, int32_t L, int32_t k, int32_t* out,
                                            OutMap m, int32_t pages, int32_t* pt_smem, int G,
                                            int rank, uint32_t* hist, uint32_t* mhist, uint2* buf,
-                                           uint32_t cap, Ctl& ctl) {
+                                           uint32_t cap, Ctl& ctl, int start_shift = 32,
+                                           uint32_t start_prefix = 0) {
   const int tid = threadIdx.x;
   if constexpr (form_of(F) == kPaged) {
     if (pages > 0 && m.pt_smem == nullptr) {  // the fast tier did not run
@@ -1461,7 +1476,62 @@ __device__ __forceinline__ void exact_tier(const Slice& s, int32_t L, int32_t k,
   uint32_t cnt = static_cast<uint32_t>(L);   // elements whose key >> shift == prefix
   uint32_t above_local = 0;                  // this CTA's elements above the bin
   uint32_t tie_local = 0;                    // this CTA's elements in the bin
-  for (;;) {
+  bool more = true;                          // another round is needed
+  if (start_shift < 32) {
+    // the window's round: keys >> start_shift above start_prefix are counted, keys equal
+    // to it go to the histogram of their next w bits
+    const int w = min(kRowRoundBits, start_shift);
+    const int nshift = start_shift - w;
+    const uint32_t mask = (1u << w) - 1u;
+    uint32_t a = 0, in = 0;
+    visit_keys(s, [&](bool ok, uint32_t key, int32_t) {
+      const uint32_t hi = key >> start_shift;
+      if (ok && hi == start_prefix) {
+        atomicAdd(&hist[hist_index(static_cast<int>((key >> nshift) & mask))], 1u);
+        ++in;
+      }
+      a += static_cast<uint32_t>(ok && hi > start_prefix);
+    });
+    const uint32_t a_cta = block_sum(a, ctl);
+    const uint32_t in_cta = block_sum(in, ctl);
+    uint32_t a_row = a_cta, in_row = in_cta;
+    if (G > 1) {  // every CTA gets every CTA's two counts
+      if (tid < G) {
+        dsmem_st(map_rank(smem_addr(&ctl.xa[rank]), tid), a_cta);
+        dsmem_st(map_rank(smem_addr(&ctl.xt[rank]), tid), in_cta);
+      }
+      cluster_sync();
+      a_row = 0;
+      in_row = 0;
+      for (int r = 0; r < G; ++r) {
+        a_row += ctl.xa[r];
+        in_row += ctl.xt[r];
+      }
+    }
+    if (a_row < need && need <= a_row + in_row) {  // the k-th key is in the window
+      need -= a_row;
+      const Sel sel = threshold_of(hist, mhist, 1 << w, need, G, rank, ctl);
+      if (G == 1) {
+        above_local = a_cta + sel.above;
+        tie_local = sel.count;
+      } else {
+        uint32_t part = 0;
+        for (int i = tid; i <= static_cast<int>(mask); i += kThreads)
+          part += static_cast<uint32_t>(i) > sel.t ? hist[hist_index(i)] : 0u;
+        tie_local = hist[hist_index(static_cast<int>(sel.t))];
+        above_local = a_cta + block_sum(part, ctl);
+      }
+      need -= sel.above;
+      prefix = (start_prefix << w) | sel.t;
+      shift = nshift;
+      cnt = sel.count;
+      more = cnt > cap && shift != 0;
+    } else {  // not: the rounds from the top bits (mhist is still zero)
+      for (int i = tid; i < hist_index(static_cast<int>(mask) + 1); i += kThreads) hist[i] = 0;
+      __syncthreads();
+    }
+  }
+  while (more) {
     const int w = min(kRowRoundBits, shift);
     const int nshift = shift - w;
     const uint32_t mask = (1u << w) - 1u;
@@ -1489,7 +1559,7 @@ __device__ __forceinline__ void exact_tier(const Slice& s, int32_t L, int32_t k,
     prefix = (prefix << w) | sel.t;
     shift = nshift;
     cnt = sel.count;
-    if (cnt <= cap || shift == 0) break;
+    more = cnt > cap && shift != 0;
   }
 
   const uint32_t k_above = static_cast<uint32_t>(k) - need;  // winners above the bin
@@ -2259,8 +2329,18 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     }
   }
 
-  // ---------------- exact tier (hist and, for CTA 0, mhist are zero here)
-  exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl);
+  // ---------------- exact tier (hist and, for CTA 0, mhist are zero here); a row whose
+  // sample predicted an overflowing filter starts from the sample's window
+  int x_start = 32;
+  uint32_t start_prefix = 0;
+  if constexpr ((F & kSingle) == 0) {
+    if (p.use_filter && static_cast<uint32_t>(L) > cap && ctl.skip_fast != 0u) {
+      x_start = static_cast<int>(ctl.ex_shift);
+      start_prefix = x_start < 32 ? ctl.lambda >> x_start : 0u;
+    }
+  }
+  exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl, x_start,
+                start_prefix);
 }
 
 // ------------------------------------------------------------------ chip-wide split
@@ -2466,8 +2546,19 @@ __device__ __forceinline__ void split_select_row(const Params& p, int row, int G
       cluster_sync();  // every CTA running, its histograms cleared
     else
       __syncthreads();
+    // too many candidates: the k-th key is at or above lambda and most likely within the
+    // candidate bins' span, [lambda, lambda + 2^(shift + kCandBits - 1)), so the exact
+    // tier starts from the bits that this span's ends share
+    int x_start = 32;
+    uint32_t x_prefix = 0;
+    if (over || total > gcap) {
+      const uint64_t end = static_cast<uint64_t>(lh.x) + (1ull << (lh.y + kCandBits - 1)) - 1;
+      const uint32_t hi = end > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(end);
+      x_start = 32 - __clz(lh.x ^ hi);
+      x_prefix = x_start < 32 ? lh.x >> x_start : 0u;
+    }
     exact_tier<F>(make_slice(rowp, L, rank, G), L, k, out, m, pages, pt_smem, G, rank, hist, mhist,
-                  buf, min(gcap, static_cast<uint32_t>(kTieCapMax)), ctl);
+                  buf, min(gcap, static_cast<uint32_t>(kTieCapMax)), ctl, x_start, x_prefix);
     return;
   }
   if (rank != 0) return;  // CTA 0 selects

@@ -404,6 +404,39 @@ def test_misleading_sample_falls_back(pkg, split):
     assert_parity(w, got)
 
 
+@pytest.mark.parametrize("tie_cap", [None, 300])
+@pytest.mark.parametrize("split", [2, 8, 16, "chip"])
+def test_misleading_sample_window_falls_back(pkg, split, tie_cap):
+    """Rows packed into a few values send a cluster row (and a chip-wide split row whose
+    candidates overflow) to the exact tier, whose first round looks only at the sample's
+    window of keys. Here the sample is wrong on purpose, and the rounds must start again
+    from the top bits. Each CTA of a cluster samples runs of 32 quads at a power-of-two
+    spacing of at least 256 quads (for these rows and splits; 1024 in the chip-wide
+    split's filter), so quads at offsets 32 .. 63 of every 64 are never sampled.
+    Row 0: constant 5.0 with 65536 larger values off the sample (the k-th key is above
+    the window). Row 1: the same with 8192 larger values. Row 2: 1024 larger values,
+    all on the sample (the window is above the k-th key). Row 3: a 'narrow' row, whose
+    window is right."""
+    batch, stride, k = 4, 262144, 2048
+    g = workloads.rng(900 + (split if split != "chip" else 1))
+    scores = np.full((batch, stride), 5.0, np.float32)
+    q = np.arange(stride // 4)
+    off_sample = [q[(q % 64 >= 32) & (q % 64 < 48)], q[(q % 256 >= 32) & (q % 256 < 40)]]
+    for b, quads in enumerate(off_sample):
+        for c in range(4):
+            scores[b, quads * 4 + c] = 6.0 + 1e-3 * g.standard_normal(quads.shape[0]).astype(np.float32)
+    on_sample = q[(q % 512 == 0) | (q % 512 == 16)]
+    for c in range(4):
+        scores[2, on_sample * 4 + c] = 6.0 + 1e-3 * g.standard_normal(on_sample.shape[0]).astype(np.float32)
+    scores[3] = workloads.random_rows(g, 1, stride, "narrow")[0]
+    seq = np.full(batch, stride, np.int32)
+    w = workloads.Workload("misleading_sample_window", "raw", k, scores, seq)
+    with (settings(pkg, chip=2, tie_cap=tie_cap) if split == "chip"
+          else settings(pkg, split=split, tie_cap=tie_cap)):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got)
+
+
 @pytest.mark.parametrize("form", ["raw", "paged"])
 @pytest.mark.parametrize("batch", [1, 64, 256])
 def test_exact_tier_alone_on_decode_sweep(pkg, batch, form):
