@@ -2263,6 +2263,8 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
     __syncthreads();
 
   // ---------------- fast tier
+  uint32_t lam_x = 0, shift_x = 0;  // lambda and its candidate-bin width, kept for the exact tier
+  bool overflow = false;            // the filter found more candidates than the buffer holds
   if (p.use_filter) {
     uint32_t shift2 = 32 - kCandBits;  // rows that skip the sample: the top key bits
     // rows split over a cluster (the long rows of the adversarial workloads) let the
@@ -2272,6 +2274,8 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
         sampled ? sample_lambda(sm, s, sample_loaded, L, static_cast<uint32_t>(k), G, rank, hist,
                                 mhist, ctl, &shift2, cap, kPredict)
                 : 0u;
+    lam_x = lambda;
+    shift_x = shift2;
     if (!(kPredict && sampled && ctl.skip_fast != 0u)) {  // else the exact tier at once
       if constexpr (form_of(F) == kPaged) {
         if (pages > 0) {
@@ -2310,6 +2314,7 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
           count_candidates(buf, n_cand, lambda, shift2, chist);
 
       }
+      overflow = n_cand > cap;
       if (__builtin_expect(n_cand >= static_cast<uint32_t>(k) && n_cand <= cap, 1)) {
         if (rank == 0)
           select_candidates<F>(buf, n_cand, static_cast<uint32_t>(k), chist, lambda, shift2, list,
@@ -2330,13 +2335,22 @@ __device__ __forceinline__ void row_body(const Params& p, int row, int G, int ra
   }
 
   // ---------------- exact tier (hist and, for CTA 0, mhist are zero here); a row whose
-  // sample predicted an overflowing filter starts from the sample's window
+  // sample predicted an overflowing filter starts from the sample's window, and a
+  // single-CTA row whose filter overflowed from the bits that the ends of its candidate
+  // bins' span, [lambda, lambda + 2^(shift + kCandBits - 1)), share
   int x_start = 32;
   uint32_t start_prefix = 0;
   if constexpr ((F & kSingle) == 0) {
     if (p.use_filter && static_cast<uint32_t>(L) > cap && ctl.skip_fast != 0u) {
       x_start = static_cast<int>(ctl.ex_shift);
       start_prefix = x_start < 32 ? ctl.lambda >> x_start : 0u;
+    }
+  } else {
+    if (overflow) {
+      const uint64_t end = static_cast<uint64_t>(lam_x) + (1ull << (shift_x + kCandBits - 1)) - 1;
+      const uint32_t hi = end > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(end);
+      x_start = 32 - __clz(lam_x ^ hi);
+      start_prefix = x_start < 32 ? lam_x >> x_start : 0u;
     }
   }
   exact_tier<F>(s, L, k, out, m, pages, pt_smem, G, rank, hist, mhist, buf, cap, ctl, x_start,

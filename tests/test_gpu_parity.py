@@ -437,6 +437,35 @@ def test_misleading_sample_window_falls_back(pkg, split, tie_cap):
     assert_parity(w, got)
 
 
+@pytest.mark.parametrize("cta,tie_cap", [(None, None), (None, 300), (256, None)])
+@pytest.mark.parametrize("batch", [8, 160])
+def test_single_cta_overflow_window(pkg, batch, cta, tie_cap):
+    """Single-CTA rows whose filter overflows start the exact tier from the bits that the
+    ends of the candidate bins' span share; here that window is wrong on purpose in half
+    the rows. A single CTA samples runs of 32 quads at a spacing of 512 quads (32768
+    elements, either build), so quads at offsets 32 .. 47 of every 64 are never sampled.
+    Rows 0 and 1: N(0, 1) and constant 5.0, each with 8192 values near 6.0 off the sample
+    (the k-th key is above the window). Rows 2 and 3: 'banded' and 'narrow' rows. 160 rows
+    take the filter that reads candidate values back from L1."""
+    stride, k = 32768, 1024
+    g = workloads.rng(960 + batch)
+    base = np.stack([g.standard_normal(stride).astype(np.float32),
+                     np.full(stride, 5.0, np.float32),
+                     workloads.random_rows(g, 1, stride, "banded")[0],
+                     workloads.random_rows(g, 1, stride, "narrow")[0]])
+    q = np.arange(stride // 4)
+    off = q[(q % 64 >= 32) & (q % 64 < 48)]
+    for b in range(2):
+        for c in range(4):
+            base[b, off * 4 + c] = 6.0 + 1e-3 * g.standard_normal(off.shape[0]).astype(np.float32)
+    scores = np.ascontiguousarray(np.tile(base, (batch // 4, 1)))
+    seq = np.full(batch, stride, np.int32)
+    w = workloads.Workload("single_cta_overflow_window", "raw", k, scores, seq)
+    with settings(pkg, split=1, staged=0, cta=cta, tie_cap=tie_cap):
+        got = run_gpu(pkg, w)
+    assert_parity(w, got, check_rows=8)
+
+
 @pytest.mark.parametrize("form", ["raw", "paged"])
 @pytest.mark.parametrize("batch", [1, 64, 256])
 def test_exact_tier_alone_on_decode_sweep(pkg, batch, form):
